@@ -1,0 +1,565 @@
+#!/usr/bin/env python3
+"""Benchmark of the ZeRO-3 per-step shard data path (libzs) on GB300.
+
+One step = reduce-scatter of every bucket of N virtual ranks (with the norm
+partial sums) -> global norm and clip coefficient -> Adam(W) + bf16 cast of
+every shard element -> the gathered parameters written into model flat
+space; all gradients resident in HBM before the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...      # the CPU oracle, same metric
+
+Prints one JSON line (rank 0).  With --gpus N > 1 (torchrun, one process
+per GPU) every GPU runs its own complete replica of the workload: the path
+has no exchange between GPUs (the N virtual ranks live in one GPU's HBM),
+so the job's throughput is the sum of the replicas' and scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO-3 shard step: params/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "params/s"
+DEFAULT_WORKLOAD = "llama3_8b"
+KERNELS_PER_STEP = 4   # reduce-scatter (all buckets), norm level 1, norm finish, Adam+gather
+
+
+def _align8(x: int) -> int:
+    return (x + 7) // 8 * 8
+
+
+def load_workload(name: str):
+    from synth import workloads
+    return workloads.WORKLOADS[name]()
+
+
+# ------------------------------------------------------------- device -----
+class DeviceWorkload:
+    """All buffers of one workload on one GPU, inputs resident.
+
+    Gradients: rank k's buffer of bucket b is a view into one gradient pool
+    filled by the synthetic generator (synth.gpu); pool_offsets lays the
+    buffers out one after another and wraps when the pool is smaller than a
+    whole step's gradients (the reuse distance is then the full pool, far
+    above the 129 MB L2, so every read comes from HBM).
+    """
+
+    def __init__(self, w, device="cuda:0", max_norm=None, pool_elems=None, seed=None):
+        import torch
+
+        import zero_sharded_optimizer_bucket_gb300 as zs
+        from synth import gpu as sg
+        from synth import workloads as wl
+
+        self.torch, self.zs, self.w = torch, zs, w
+        self.dev = torch.device(device)
+        self.seed = w.seed if seed is None else seed
+        self.max_norm = w.max_norm if max_norm is None else max_norm
+        cfg = zs.zs_default_config(w.n_ranks)
+        cfg.param_persistence_threshold = w.persistence_threshold
+        cfg.reduce_bucket_size = w.reduce_bucket_size
+        cfg.prefetch_bucket_size = w.prefetch_bucket_size
+        cfg.sub_group_size = w.sub_group_size
+        self.plan = zs.zs_build_partition(cfg, w.numel, w.ds_id)
+        info = self.info = zs.zs_plan_info(self.plan)
+        N, S, Pn = info["n_ranks"], info["shard_elems"], info["persist_elems"]
+        self.N = N
+        E = lambda n, dt: torch.empty(max(int(n), 8), dtype=dt, device=self.dev)
+        self.table = E(info["device_table_bytes"], torch.uint8)
+        zs.zs_plan_upload(self.plan, self.table, self.table.numel())
+        self.gs, self.ps = E(N * S, torch.int16), E(N * S, torch.int16)
+        self.master, self.m, self.v = (E(N * S, torch.float32) for _ in range(3))
+        self.gP, self.pP = E(Pn, torch.int16), E(Pn, torch.int16)
+        self.pm, self.pmm, self.pmv = (E(Pn, torch.float32) for _ in range(3))
+        self.state = zs.make_state(grad_shards=self.gs, param_shards=self.ps, master=self.master,
+                                   exp_avg=self.m, exp_avg_sq=self.v, persist_grads=self.gP,
+                                   persist_params=self.pP, p_master=self.pm, p_exp_avg=self.pmm,
+                                   p_exp_avg_sq=self.pmv)
+        self.scratch = E(info["norm_scratch_elems"], torch.float64)
+        self.d_norm = torch.zeros(8, dtype=torch.float32, device=self.dev)
+        self.d_coef = torch.zeros(8, dtype=torch.float32, device=self.dev)
+        self.d_flags = torch.zeros(8, dtype=torch.int32, device=self.dev)
+        self.flat = E(info["flat_elems"], torch.int16)
+        self.hp = w.hparams()
+        self.t = 0
+        # weights: full fp32 parameters from the generator, partitioned once
+        W = E(info["psi"], torch.float32)
+        sg.fill_weight_f32(W, 0, self.seed, w.weight_sigma)
+        zs.zs_partition(self.plan, W, self.state)
+        torch.cuda.synchronize(self.dev)
+        del W
+        # gradient pool
+        nb = info["n_reduce_buckets"]
+        self.buf_elems = [zs.zs_bucket_info(self.plan, b)["buf_elems"] for b in range(nb)]
+        total = sum(N * _align8(L) for L in self.buf_elems)
+        if pool_elems is None:
+            free = torch.cuda.mem_get_info(self.dev)[0]
+            cap = max((free - (6 << 30)) // 2, 0)
+            pool_elems = min(total, cap)
+        need = (N + 1) * _align8(max(self.buf_elems, default=8))
+        pool_elems = max(int(pool_elems), min(need, total) if total else 8)
+        if total and pool_elems < total:
+            pool_elems = max(pool_elems, need)
+        self.pool = E(pool_elems, torch.int16)
+        sg.fill_grad_bf16(self.pool, 0, self.seed, w.grad_sigma, w.outlier_frac, w.outlier_scale)
+        self.pool_elems = self.pool.numel()
+        self.offs = wl.pool_offsets(self.buf_elems, N, self.pool_elems) if nb else []
+        base = self.pool.data_ptr()
+        flat_ptrs = [base + 2 * o for row in self.offs for o in row]
+        self.ptr_table = torch.tensor(flat_ptrs or [0], dtype=torch.int64, device=self.dev)
+        torch.cuda.synchronize(self.dev)
+
+    # host-side view of rank pointers of one bucket
+    def bucket_ptrs(self, b):
+        base = self.pool.data_ptr()
+        return [base + 2 * o for o in self.offs[b]]
+
+    def step(self, stream=None):
+        self.t += 1
+        self.zs.zs_shard_step(self.plan, self.ptr_table, self.state, self.scratch, self.hp, self.t,
+                              self.max_norm, self.d_norm, self.d_coef, self.d_flags, self.flat,
+                              stream)
+
+    def step_timed(self, ev):
+        """The same step as step(), as its three calls with events between."""
+        zs = self.zs
+        self.t += 1
+        ev[0].record()
+        zs.zs_reduce_scatter_all(self.plan, self.ptr_table, self.gs, self.gP, self.scratch)
+        ev[1].record()
+        zs.zs_grad_norm(self.plan, self.gs, self.gP, self.scratch, False, self.max_norm,
+                        self.d_norm, self.d_coef, self.d_flags)
+        ev[2].record()
+        zs.zs_adam_gather(self.plan, self.hp, self.t, self.d_coef, self.d_flags, self.state,
+                          self.flat)
+        ev[3].record()
+
+    def algorithmic_bytes(self):
+        """Bytes the method must move per step (padding excluded):
+        reduce-scatter 2N + 2 per element; Adam + cast 28 per element plus
+        2 for the gathered write of partitioned elements."""
+        psi, N = self.info["psi"], self.N
+        part = psi - self.info["persist_elems_logical"]
+        rs = (2 * N + 2) * psi
+        ag = 28 * psi + 2 * part
+        norm = 8 * self.info["n_tiles"] * 2
+        return {"reduce_scatter": rs, "norm": norm, "adam_gather": ag}
+
+
+# ------------------------------------------------------------- clocks -----
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.proc, self.path, self.gpu_id = None, None, gpu_id
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader", "-lms", "200"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1].split()[0]), float(parts[2].split()[0]), parts))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, p in rows for n, v in zip(names, p[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------- helpers ------
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, when
+    it was taken on the kernel sources as they are now (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel)
+    if not ent or ent.get("sources_sha256") != sources_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "zero_sharded_optimizer_bucket_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (x itself when world == 1)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------ CPU baseline ------
+def _sample_params(w, target=4_200_000):
+    """A bounded sample of the workload: the smallest run of parameters in
+    ds_id order, each at most 8M elements, reaching `target` elements."""
+    idx, tot = [], 0
+    for i, n in enumerate(w.numel):
+        if n <= 8_000_000:
+            idx.append(i)
+            tot += n
+            if tot >= target:
+                break
+    return idx
+
+
+def oracle_step_timer(w, sample_idx, bufs_fn, budget_s, min_steps=1):
+    """Time the oracle's whole step on the sampled parameters."""
+    import numpy as np
+
+    from oracle import plan as oplan
+    from oracle import step as ostep
+    from synth import philox
+    numel = [w.numel[i] for i in sample_idx]
+    plan = oplan.build_partition(numel, w.n_ranks, threshold=w.persistence_threshold,
+                                 reduce_bucket_size=w.reduce_bucket_size,
+                                 prefetch_bucket_size=w.prefetch_bucket_size,
+                                 sub_group_size=w.sub_group_size)
+    W = philox.weight_f32(w.seed, np.arange(plan.input_elems, dtype=np.uint64), w.weight_sigma)
+    st = ostep.partition(plan, W)
+    bufs = bufs_fn(plan)
+    times, t = [], 0
+    t_start = time.perf_counter()
+    while len(times) < min_steps or time.perf_counter() - t_start < budget_s:
+        t += 1
+        t0 = time.perf_counter()
+        ostep.shard_step(plan, st, bufs, w.hparams(), t, w.max_norm)
+        times.append(time.perf_counter() - t0)
+    return plan, times
+
+
+def cpu_baseline(w, dw=None, budget_s=12.0):
+    import numpy as np
+    idx = _sample_params(w)
+    N = w.n_ranks
+
+    def bufs_from_device(plan):
+        # inputs for a timing run: gradient buffers copied from the device pool
+        out, off = [], 0
+        pool = dw.pool
+        for L in plan.bucket_buf_elems:
+            row = []
+            for _ in range(N):
+                L8 = _align8(L)
+                if off + L8 > pool.numel():
+                    off = 0
+                row.append(pool[off:off + L].cpu().numpy().view(np.uint16).copy())
+                off += L8
+            out.append(row)
+        return out
+
+    plan, times = oracle_step_timer(w, idx, bufs_from_device, budget_s)
+    sample_psi = plan.psi
+    per = statistics.median(times)
+    return {"value": sample_psi / per, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(idx)} parameters of {w.name} ({sample_psi} elements, N={N}, "
+                      f"{len(plan.reduce_buckets)} reduce buckets): whole oracle step, "
+                      f"{len(times)} steps, median {per:.3f} s, numpy float32 on one core"}
+
+
+# ------------------------------------------------------------- e2e --------
+def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
+    """Same step through the C ABI with the gradients arriving from pinned
+    host memory every step: per bucket one host->device copy of the N rank
+    buffers into a ring of device slots (copy stream), zs_reduce_scatter on
+    the compute stream as soon as its slot is filled, then zs_grad_norm and
+    zs_adam_gather, and the norm and flag word read back to the host."""
+    torch, zs = dw.torch, dw.zs
+    from synth import workloads as wl
+    N, nb = dw.N, len(dw.buf_elems)
+    if nb == 0:
+        return None
+    sizes = [N * _align8(L) for L in dw.buf_elems]
+    total = sum(sizes)
+    H = min(total, max(host_pool_bytes // 2, 2 * max(sizes)))
+    host = torch.empty(H, dtype=torch.int16, pin_memory=True)
+    host.copy_(dw.pool[:min(H, dw.pool.numel())].cpu()) if H <= dw.pool.numel() else host.zero_()
+    hoffs = [row[0] for row in wl.pool_offsets(sizes, 1, H)]
+    smax = max(sizes)
+    ring = torch.empty(slots * smax, dtype=torch.int16, device=dw.dev)
+    cs = torch.cuda.Stream(device=dw.dev)
+    comp = torch.cuda.current_stream(dw.dev)
+    filled = [torch.cuda.Event() for _ in range(slots)]
+    free = [torch.cuda.Event() for _ in range(slots)]
+    out = torch.empty(2, dtype=torch.int32, pin_memory=True)
+    h2d = sum(2 * N * L for L in dw.buf_elems)
+
+    def one_step():
+        dw.t += 1
+        for b in range(nb):
+            s = b % slots
+            n = sizes[b]          # the N rank buffers of the bucket, back to back
+            if b >= slots:
+                cs.wait_event(free[s])
+            with torch.cuda.stream(cs):
+                ring[s * smax:s * smax + n].copy_(host[hoffs[b]:hoffs[b] + n], non_blocking=True)
+                filled[s].record(cs)
+            comp.wait_event(filled[s])
+            base = ring.data_ptr() + 2 * s * smax
+            ptrs = [base + 2 * k * _align8(dw.buf_elems[b]) for k in range(N)]
+            zs.zs_reduce_scatter(dw.plan, b, ptrs, dw.gs, dw.gP, dw.scratch)
+            free[s].record(comp)
+        zs.zs_grad_norm(dw.plan, dw.gs, dw.gP, dw.scratch, False, dw.max_norm, dw.d_norm,
+                        dw.d_coef, dw.d_flags)
+        zs.zs_adam_gather(dw.plan, dw.hp, dw.t, dw.d_coef, dw.d_flags, dw.state, dw.flat)
+        out[0:1].copy_(dw.d_norm[0:1].view(torch.int32), non_blocking=True)
+        out[1:2].copy_(dw.d_flags[0:1], non_blocking=True)
+        comp.synchronize()
+
+    for _ in range(warmup):
+        one_step()
+    torch.cuda.synchronize(dw.dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": dw.info["psi"] / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": 8, "ms_per_step": dt * 1e3, "steps": steps,
+            "path": "pinned host gradients -> per-bucket H2D ring -> zs_reduce_scatter; "
+                    "zs_grad_norm; zs_adam_gather; norm+flags D2H"}
+
+
+# ----------------------------------------------------------- arms ---------
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = load_workload(args.workload)
+    dw = DeviceWorkload(w, dev)
+    for _ in range(args.warmup):
+        dw.step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(_gpu_uuid(torch, dev))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.25)
+    for k in range(K):
+        dw.step_timed(evs[k])
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ck = clocks.stop()
+    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    step_ms = max_over_ranks(total_ms / K, world)
+    per = {"reduce_scatter": [e[0].elapsed_time(e[1]) for e in evs],
+           "norm": [e[1].elapsed_time(e[2]) for e in evs],
+           "adam_gather": [e[2].elapsed_time(e[3]) for e in evs]}
+    avg = {k: sum(v) / len(v) for k, v in per.items()}
+    alg = dw.algorithmic_bytes()
+    dom = max(("reduce_scatter", "adam_gather"), key=lambda k: avg[k])
+    peak, peak_kind = peaks()
+    achieved = alg[dom] / (avg[dom] * 1e-3) / 1e9
+    psi = dw.info["psi"]
+    value = world * psi / (step_ms * 1e-3)
+    step_bytes = alg["reduce_scatter"] + alg["adam_gather"]
+    flags = int(dw.d_flags[0].item())
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
+        "data": "synthetic (Philox4x32-10 gradients and weights; architecture shapes only)",
+        "config": {"workload": w.name, "n_ranks": w.n_ranks, "psi": psi,
+                   "n_params": w.n_params, "reduce_bucket_size": w.reduce_bucket_size,
+                   "prefetch_bucket_size": w.prefetch_bucket_size,
+                   "param_persistence_threshold": w.persistence_threshold,
+                   "max_norm": dw.max_norm,
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.1f} GB moved per step, "
+                         f"gradient pool {2 * dw.pool_elems / 1e9:.1f} GB",
+                   "parallelism": "replicas" if world > 1 else "single GPU, N virtual ranks"},
+        "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+        "hbm_frac_of_measured": step_bytes / (step_ms * 1e-3) / 1e9 / peak,
+        "kernel_ms": avg,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(dom),
+                     "algorithmic_bytes_per_launch": alg[dom]},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": ck,
+        "skip_flags": flags,
+    }
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(dw, steps=args.e2e_steps)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, dw, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, same metric and workload:
+    each step is the oracle's whole step on a bounded sample of the
+    workload's parameters (inputs drawn on the CPU by synth.philox)."""
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+
+    from synth import philox
+    w = load_workload(args.workload)
+    idx = _sample_params(w, target=2_000_000)
+    N = w.n_ranks
+
+    def bufs_cpu(plan):
+        out, run = [], 0
+        for L in plan.bucket_buf_elems:
+            row = []
+            for _ in range(N):
+                row.append(philox.grad_bf16(w.seed, 0, np.arange(run, run + L, dtype=np.uint64),
+                                            w.grad_sigma, w.outlier_frac, w.outlier_scale))
+                run += _align8(L)
+            out.append(row)
+        return out
+
+    from oracle import plan as oplan
+    from oracle import step as ostep
+    numel = [w.numel[i] for i in idx]
+    plan = oplan.build_partition(numel, N, threshold=w.persistence_threshold,
+                                 reduce_bucket_size=w.reduce_bucket_size,
+                                 prefetch_bucket_size=w.prefetch_bucket_size,
+                                 sub_group_size=w.sub_group_size)
+    Wt = philox.weight_f32(w.seed, np.arange(plan.input_elems, dtype=np.uint64), w.weight_sigma)
+    st = ostep.partition(plan, Wt)
+    bufs = bufs_cpu(plan)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        ostep.shard_step(plan, st, bufs, w.hparams(), t, w.max_norm)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t += 1
+        ostep.shard_step(plan, st, bufs, w.hparams(), t, w.max_norm)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = plan.psi / dt
+    sample = (f"{len(idx)} parameters of {w.name} ({plan.psi} elements, N={N}): whole oracle "
+              f"step per timed step, numpy float32, one core")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": w.name, "n_ranks": N, "psi": w.psi,
+                                        "sample_psi": plan.psi},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="zs", choices=["zs", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "zs":
+        print("bench.py: at least 3 warm-up steps are required", file=sys.stderr)
+        return 2
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

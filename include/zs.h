@@ -1,0 +1,345 @@
+/*
+ * zs.h — C ABI of libzs: the ZeRO-3 per-step shard data path on one GPU.
+ *
+ * N data-parallel ranks are *virtual*: all of their buffers live in the HBM
+ * of one GPU, and the collectives of the method (reduce-scatter of the
+ * gradient buckets, the scalar all-reduce of the gradient norm, the
+ * coalesced all-gather of the parameters) are kernels over those buffers.
+ *
+ * Sources (page title, then the section on it):
+ *   [ZeRO-3 chapter] "03 · ZeRO-3：参数分片与 all-gather 调度"
+ *   [Grok blog]      "DeepSpeed ZeRO Stage 3：参数分区，让大模型训练“零负担”"
+ *   [Core flow]      "ZeRO-3 核心流程：把参数也切开的那一档"
+ *
+ * Conventions
+ * -----------
+ * - Every entry point returns a zs_status; ZS_OK is 0.  Argument errors are
+ *   found on the host, return ZS_EINVAL and enqueue nothing.  A CUDA error
+ *   returns ZS_ECUDA.  No call aborts or exits; zs_last_error() gives a
+ *   message for the calling thread.
+ * - Device buffers are owned by the caller; the library allocates no device
+ *   memory.  The plan is host memory owned by the library (zs_free_plan).
+ * - Device work is enqueued on the caller's cudaStream_t (passed as void*,
+ *   NULL = legacy default stream).  No call synchronises the host with the
+ *   device; results such as the gradient norm stay in device memory.
+ * - bf16 buffers hold IEEE bfloat16 bit patterns (2 bytes per element).
+ * - Device buffers read or written with 16-byte vectors must be 16-byte
+ *   aligned: every buffer except the flat output of the gathers, which needs
+ *   only 2-byte alignment.  Misalignment is ZS_EINVAL.
+ *
+ * Layouts (elements; "ds_id order" = parameters sorted by ds_id)
+ * --------------------------------------------------------------
+ * ps_p      = ceil(numel_p / N): rank r owns flat elements
+ *             [r*ps_p, (r+1)*ps_p) of parameter p, zero beyond numel_p
+ *             ([ZeRO-3 chapter] §3.1, item 1).
+ * persistent: numel_p < param_persistence_threshold; never partitioned
+ *             ([ZeRO-3 chapter] §5.3, last paragraph).
+ * shard space      [N][S]: row r holds rank r's shards of all partitioned
+ *             parameters; p at columns [S_p, S_p+ps_p), S_p = running sum
+ *             of ps rounded up to a multiple of 8.  Gradient shards, 16-bit
+ *             parameter shards and the fp32 master / exp_avg / exp_avg_sq
+ *             shards all use it ([ZeRO-3 chapter] §6.1: one flat buffer of
+ *             gradient partitions, fp32 partitions per rank).
+ * persistent space [Pn]: persistent parameters whole, once, at P_p =
+ *             running sum of numel rounded up to 8.
+ * model flat space: partitioned parameters gathered, back to back in ds_id
+ *             order, each its N shards in rank order (N*ps_p elements, the
+ *             first numel_p of which are the parameter), at F_p = running
+ *             sum of N*ps ([ZeRO-3 chapter] §5.2, all_gather_coalesced).
+ * input space: all parameters whole, back to back in ds_id order at W_p =
+ *             running sum of numel (the weights handed to zs_partition).
+ * reduce bucket buffer: one per rank and bucket; the bucket's entries
+ *             (a parameter, or a chunk [c*B,(c+1)*B) of a parameter larger
+ *             than B = reduce_bucket_size) back to back, each starting at a
+ *             multiple of 8; buf_elems (zs_bucket_info_t) elements, a multiple
+ *             of 8.  Rank k's buffer holds rank k's gradient (bf16).
+ */
+#ifndef ZS_H
+#define ZS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t zs_status;
+#define ZS_OK        0
+#define ZS_EINVAL   (-1)   /* bad argument: nothing was enqueued            */
+#define ZS_ENOMEM   (-2)   /* host allocation failed                        */
+#define ZS_ECUDA    (-3)   /* a CUDA call failed (message names it)         */
+#define ZS_ESTATE   (-4)   /* call out of order (e.g. plan not uploaded)    */
+#define ZS_ETIMEOUT (-5)   /* reserved: no entry point waits on the device  */
+
+/* Largest N the per-bucket reduce-scatter accepts (its rank pointers travel
+ * as kernel arguments). */
+#define ZS_MAX_RANKS 256
+
+/* Bits of the device flag word written by zs_grad_norm / zs_shard_step. */
+#define ZS_SKIP_NONFINITE 1   /* gradient norm not finite: update skipped */
+
+typedef struct zs_plan zs_plan;   /* opaque, host memory */
+
+/* Defaults: the DeepSpeed ZeRO-3 values quoted on the pages —
+ * stage3_param_persistence_threshold 1e5, reduce_bucket_size 5e6,
+ * stage3_prefetch_bucket_size 5e7 ([Core flow] §4 config block;
+ * [ZeRO-3 chapter] §5.2, §5.3), sub_group_size 1e9 ([ZeRO-3 chapter] §6.1,
+ * counted in per-rank shard elements). */
+typedef struct {
+    int32_t n_ranks;                      /* N >= 1                              */
+    int32_t reserved;                     /* must be 0                           */
+    int64_t param_persistence_threshold;  /* persistent iff numel < threshold    */
+    int64_t reduce_bucket_size;           /* elements, >= 1                      */
+    int64_t prefetch_bucket_size;         /* elements, >= 1 (gather buckets)     */
+    int64_t sub_group_size;               /* per-rank elements, >= 1             */
+} zs_config;
+
+typedef struct {
+    float   lr, beta1, beta2, eps, weight_decay;
+    int32_t adamw;            /* 1: decoupled decay (AdamW); 0: L2 into the gradient */
+    int32_t bias_correction;  /* 1: divide the moments by 1-beta^t                   */
+} zs_adam_hparams;
+
+typedef struct {
+    int32_t n_ranks, n_params;
+    int32_t n_reduce_buckets, n_gather_buckets;
+    int32_t n_sub_groups, reserved;
+    int64_t psi;                    /* sum of numel                                   */
+    int64_t shard_elems;            /* S: length of one shard row (multiple of 8)     */
+    int64_t shard_elems_logical;    /* sum of ps over partitioned parameters          */
+    int64_t persist_elems;          /* length of persistent space (multiple of 8)     */
+    int64_t persist_elems_logical;  /* sum of numel over persistent parameters        */
+    int64_t flat_elems;             /* length of model flat space                     */
+    int64_t padding_elems;          /* sum of N*ps - numel                            */
+    int64_t max_bucket_buf_elems;   /* largest reduce bucket buffer                   */
+    int64_t max_gather_elems;       /* largest gather bucket                          */
+    int64_t bytes_per_rank;         /* 16*(shard_elems_logical + persist_elems_logical) */
+    int64_t n_tiles;                /* work tiles of the kernels                      */
+    int64_t device_table_bytes;     /* device memory zs_plan_upload needs             */
+    int64_t norm_scratch_elems;     /* doubles of norm scratch the calls need         */
+} zs_plan_info_t;
+
+typedef struct {
+    int64_t numel, ds_id;
+    int64_t partition_size;   /* ps (0 for persistent)                  */
+    int64_t padding;          /* N*ps - numel (0 for persistent)        */
+    int64_t shard_offset;     /* S_p, or -1 for persistent              */
+    int64_t persist_offset;   /* P_p, or -1 for partitioned             */
+    int64_t flat_offset;      /* F_p, or -1 for persistent              */
+    int64_t input_offset;     /* W_p                                    */
+    int32_t persistent;
+    int32_t position;         /* rank of the parameter in ds_id order   */
+    int32_t sub_group;
+    int32_t gather_bucket;    /* -1 for persistent                      */
+    int32_t first_reduce_bucket;
+    int32_t n_reduce_buckets; /* > 1 when the parameter is split in chunks */
+} zs_param_info_t;
+
+typedef struct {
+    int32_t n_entries, reserved;
+    int64_t buf_elems;        /* elements of each rank's buffer (multiple of 8) */
+    int64_t grad_elems;       /* gradient elements the bucket carries           */
+    int64_t first_tile, n_tiles;
+} zs_bucket_info_t;
+
+typedef struct {
+    int32_t n_params, reserved;
+    int64_t flat_offset;      /* of the bucket in model flat space */
+    int64_t flat_elems;
+} zs_gather_bucket_info_t;
+
+typedef struct {
+    int32_t n_params, reserved;
+    int64_t shard_lo, shard_hi;       /* shard-space columns of the sub-group */
+    int64_t persist_lo, persist_hi;   /* persistent-space range               */
+} zs_sub_group_info_t;
+
+/* Device pointers of the per-rank optimizer state and 16-bit buffers, all in
+ * the layouts above ([ZeRO-3 chapter] §6.1: per-rank fp32 partitions, the
+ * flat gradient-partition buffer; [Core flow] §1: 2 + 2 + 12 bytes per
+ * element).  Shard arrays have N*S elements, persistent arrays Pn. */
+typedef struct {
+    void  *grad_shards;      /* bf16 [N][S]  reduced gradients            */
+    void  *param_shards;     /* bf16 [N][S]  16-bit parameter shards      */
+    float *master;           /* fp32 [N][S]                               */
+    float *exp_avg;          /* fp32 [N][S]                               */
+    float *exp_avg_sq;       /* fp32 [N][S]                               */
+    void  *persist_grads;    /* bf16 [Pn]                                 */
+    void  *persist_params;   /* bf16 [Pn]                                 */
+    float *p_master;         /* fp32 [Pn]                                 */
+    float *p_exp_avg;        /* fp32 [Pn]                                 */
+    float *p_exp_avg_sq;     /* fp32 [Pn]                                 */
+} zs_shard_state;
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *zs_last_error(void);
+
+/* Library version string. */
+const char *zs_version(void);
+
+/* Fill *cfg with the defaults above for n_ranks ranks. */
+void zs_default_config(zs_config *cfg, int32_t n_ranks);
+
+/* A1 — build the partition plan ([ZeRO-3 chapter] §3.1 partition range,
+ * §5.3 persistence, §6.1 sub-groups, §6.2 reduce buckets, §5.2 gather
+ * buckets).  numel[n_params] (>= 0), ds_id[n_params] unique or NULL for
+ * index order.  Host only: no device call.  *out receives a plan owned by
+ * the caller until zs_free_plan.  n_params == 0 gives an empty plan.
+ * Errors: ZS_EINVAL (bad config, negative numel, duplicate ds_id),
+ * ZS_ENOMEM. */
+zs_status zs_build_partition(const zs_config *cfg, int32_t n_params, const int64_t *numel,
+                             const int64_t *ds_id, zs_plan **out);
+
+/* Release a plan (NULL is a no-op).  Device memory given to zs_plan_upload
+ * stays the caller's. */
+void zs_free_plan(zs_plan *plan);
+
+/* Plan queries (host only).  Index arguments out of range: ZS_EINVAL. */
+zs_status zs_plan_info(const zs_plan *plan, zs_plan_info_t *out);
+zs_status zs_param_info(const zs_plan *plan, int32_t param, zs_param_info_t *out);
+zs_status zs_param_at(const zs_plan *plan, int32_t position, int32_t *param);
+zs_status zs_bucket_info(const zs_plan *plan, int32_t bucket, zs_bucket_info_t *out);
+zs_status zs_bucket_entry(const zs_plan *plan, int32_t bucket, int32_t entry, int32_t *param,
+                          int64_t *elem_lo, int64_t *elem_hi, int64_t *buf_offset);
+zs_status zs_gather_bucket_info(const zs_plan *plan, int32_t gather_bucket,
+                                zs_gather_bucket_info_t *out);
+zs_status zs_gather_bucket_param(const zs_plan *plan, int32_t gather_bucket, int32_t i,
+                                 int32_t *param);
+zs_status zs_sub_group_info(const zs_plan *plan, int32_t sub_group, zs_sub_group_info_t *out);
+
+/* Host copy of the plan's work table (the bytes zs_plan_upload sends to the
+ * device), for inspection and tests.  The table is an array of n_tiles
+ * records of 48 bytes: int64 dst, src, flat, win; int32 len, valid,
+ * flat_len, bucket.  A tile is a run of `len` destination elements starting
+ * at `dst` in shard space (row-major [N][S]) or, when flat < 0, in
+ * persistent space; its first `valid` elements take their data from
+ * element `src` on of the bucket `bucket`'s gradient buffers and from
+ * element `win` on of input space; the rest are zero padding; its first
+ * flat_len elements also go to model flat space from element `flat` on.
+ * Errors: ZS_EINVAL (bytes < device_table_bytes). */
+zs_status zs_plan_table(const zs_plan *plan, void *host_out, int64_t bytes);
+
+/* Copy the plan's work tables to device memory owned by the caller
+ * (d_table: 16-byte aligned, >= device_table_bytes).  Enqueued on stream;
+ * the plan keeps d_table and uses it in every later device call, so it must
+ * stay allocated while the plan is used.  Calling it again moves the plan
+ * to the new buffer.  Errors: ZS_EINVAL, ZS_ECUDA. */
+zs_status zs_plan_upload(zs_plan *plan, void *d_table, int64_t bytes, void *stream);
+
+/* A1 data movement — partition full fp32 parameters (input space,
+ * input_elems = psi floats, 16-byte aligned) into every rank's fp32 master
+ * shard and bf16 parameter shard, zero padding, and the persistent
+ * parameters into persistent space; exp_avg and exp_avg_sq are zeroed
+ * ([ZeRO-3 chapter] §3.1: _partition_param copies the rank's range into
+ * ds_tensor; §6.1: _create_fp32_partitions).  grad buffers of st are not
+ * touched (may be NULL).  Errors: ZS_EINVAL, ZS_ESTATE (not uploaded),
+ * ZS_ECUDA. */
+zs_status zs_partition(const zs_plan *plan, const float *full_params, const zs_shard_state *st,
+                       void *stream);
+
+/* A2 — reduce-scatter one bucket ([ZeRO-3 chapter] §6.2: a full IPG bucket
+ * is all-reduced and each rank keeps its range, or reduce-scattered to the
+ * owners; [Grok blog] §3: sum, average, scatter).  For every element
+ * (r, S_p+j) of the bucket: s = 0; for k = 0..N-1 s += float(g_k[e]) in
+ * that order (0 for e >= numel); grad_shards[r][S_p+j] = bf16_rne(s / N).
+ * Persistent entries write persist_grads the same way on the full range.
+ * rank_grads: HOST array of N device pointers (16-byte aligned, >=
+ * buf_elems elements each).  If norm_scratch is not NULL (>=
+ * norm_scratch_elems doubles), the bucket's tiles also write their sums of
+ * squared results there for zs_grad_norm.  Errors: ZS_EINVAL (bucket out
+ * of range, N > ZS_MAX_RANKS, NULL or misaligned pointer), ZS_ESTATE,
+ * ZS_ECUDA. */
+zs_status zs_reduce_scatter(const zs_plan *plan, int32_t bucket, const void *const *rank_grads,
+                            void *grad_shards, void *persist_grads, double *norm_scratch,
+                            void *stream);
+
+/* A3 — global gradient norm and clip coefficient ([ZeRO-3 chapter] §6.3:
+ * unscale_and_clip_grads(sub_group_id, global_norm); [Core flow] 坑 1: the
+ * norm must cover all shards, each rank alone would clip differently).
+ * norm = sqrt(sum of squares of every shard element and every persistent
+ * element); coef = min(1, max_norm / (norm + 1e-6)) in fp32, 1 when
+ * max_norm <= 0 or when the norm is not finite.  recompute = 0 uses the
+ * per-tile sums that zs_reduce_scatter left in norm_scratch (every bucket
+ * must have been reduced with it since); recompute = 1 first recomputes
+ * them from grad_shards / persist_grads.  Writes device scalars d_norm,
+ * d_clip_coef and the flag word d_flags (ZS_SKIP_NONFINITE).  Errors:
+ * ZS_EINVAL, ZS_ESTATE, ZS_ECUDA. */
+zs_status zs_grad_norm(const zs_plan *plan, const void *grad_shards, const void *persist_grads,
+                       double *norm_scratch, int32_t recompute, float max_norm, float *d_norm,
+                       float *d_clip_coef, int32_t *d_flags, void *stream);
+
+/* A4 — Adam(W) on one sub-group (-1: all) of every rank's fp32 shard and
+ * of its persistent parameters, then the bf16 cast of the new master into
+ * param_shards / persist_params ([ZeRO-3 chapter] §6.3: per sub-group
+ * clip, optimizer step on the rank's fp32 partition, write back the 16-bit
+ * shard; §6.1 sub_group_size).  In fp32, per element, in this order:
+ *   g = float(grad) * coef
+ *   AdamW: p = p - (lr*wd)*p        |  Adam-L2: g = g + wd*p
+ *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
+ *   p = p - lr * ((m/bc1) / (sqrt(v/bc2) + eps));  param = bf16_rne(p)
+ * with 1-b, lr*wd, bc = 1-b^t computed in double on the host and rounded to
+ * fp32 (bc = 1 without bias correction).  step t >= 1 is the caller's
+ * counter.  d_clip_coef / d_flags are device scalars from zs_grad_norm;
+ * when d_flags has ZS_SKIP_NONFINITE set nothing is written.  Errors:
+ * ZS_EINVAL (sub_group out of range, step < 1, bad pointer), ZS_ECUDA. */
+zs_status zs_adam_step(const zs_plan *plan, int32_t sub_group, const zs_adam_hparams *hp,
+                       int64_t step, const float *d_clip_coef, const int32_t *d_flags,
+                       const zs_shard_state *st, void *stream);
+
+/* A5 — all_gather_coalesced ([ZeRO-3 chapter] §5.2: sort the group by
+ * ds_id, pack one flat buffer, one collective, per-parameter views; §7:
+ * a wrong order is silently wrong).  params[n]: parameter indices in any
+ * order, no duplicates.  Partitioned parameters are laid out in ds_id
+ * order, each as its N shards in rank order (N*ps elements, the first
+ * numel of which are the parameter); flat_out (2-byte aligned) receives
+ * them; view_offsets (HOST, n entries) receives each listed parameter's
+ * offset in flat_out, -1 for a persistent parameter (already whole, not
+ * gathered).  flat_capacity: elements available at flat_out.  The bytes
+ * equal what each of the N ranks would receive.  Errors: ZS_EINVAL
+ * (index out of range, duplicate, capacity too small), ZS_ESTATE,
+ * ZS_ECUDA. */
+zs_status zs_all_gather_coalesced(const zs_plan *plan, int32_t n, const int32_t *params,
+                                  const void *param_shards, void *flat_out,
+                                  int64_t flat_capacity, int64_t *view_offsets, void *stream);
+
+/* A2 over every bucket in one launch — the first pass of zs_shard_step.
+ * Same result as zs_reduce_scatter on each bucket in turn.  d_rank_grads
+ * as in zs_shard_step; norm_scratch (>= norm_scratch_elems doubles) receives
+ * every tile's partial sum.  Errors: ZS_EINVAL, ZS_ESTATE, ZS_ECUDA. */
+zs_status zs_reduce_scatter_all(const zs_plan *plan, const void *const *d_rank_grads,
+                                void *grad_shards, void *persist_grads, double *norm_scratch,
+                                void *stream);
+
+/* A4 + A5 in one launch — the second pass of zs_shard_step: Adam(W) and the
+ * bf16 cast of every element (all sub-groups), and each new bf16 parameter
+ * also written at its place in model flat space (flat_out, flat_elems,
+ * 2-byte aligned), as zs_all_gather_coalesced of every gather bucket would.
+ * Same arguments and skip rule as zs_adam_step.  Errors: ZS_EINVAL,
+ * ZS_ESTATE, ZS_ECUDA. */
+zs_status zs_adam_gather(const zs_plan *plan, const zs_adam_hparams *hp, int64_t step,
+                         const float *d_clip_coef, const int32_t *d_flags,
+                         const zs_shard_state *st, void *flat_out, void *stream);
+
+/* A6 — the fused step: reduce-scatter of every bucket with the norm partial
+ * sums (one launch over all tiles), the norm / clip finish, then Adam(W),
+ * the bf16 cast and the write of the gathered parameters into model flat
+ * space (one launch over all tiles).  Results are bit-identical to
+ * zs_reduce_scatter (every bucket, with norm_scratch) -> zs_grad_norm
+ * (recompute 0) -> zs_adam_step(-1) -> zs_all_gather_coalesced of every
+ * gather bucket into its place in model flat space.
+ * d_rank_grads: DEVICE array [n_reduce_buckets][N] of device pointers
+ * (rank k's buffer of bucket b at [b*N + k]; 16-byte aligned; a NULL or
+ * misaligned entry is not read and makes the norm NaN, so the update is
+ * skipped).  flat_out: model flat space (flat_elems, 2-byte aligned).
+ * Errors: ZS_EINVAL, ZS_ESTATE, ZS_ECUDA. */
+zs_status zs_shard_step(const zs_plan *plan, const void *const *d_rank_grads,
+                        const zs_shard_state *st, double *norm_scratch,
+                        const zs_adam_hparams *hp, int64_t step, float max_norm,
+                        float *d_norm, float *d_clip_coef, int32_t *d_flags,
+                        void *flat_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZS_H */

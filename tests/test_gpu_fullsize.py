@@ -1,0 +1,162 @@
+"""Full-size parity on sampled outputs, in the launch configuration bench.py
+times (bench.DeviceWorkload + zs_shard_step).
+
+The oracle computes each sampled element on its own: the N rank gradients
+of that element (drawn by synth at the element's pool position), the rank
+mean, one AdamW step from the partitioned initial weight.  max_norm = 0
+makes the clip coefficient exactly 1 on both sides, so no value computed by
+the device is ever an input of the oracle.  The gradient norm at full size
+is checked through a property that holds at any size: it equals the norm
+of the device's reduced-gradient buffers (float64 sum).
+"""
+from __future__ import annotations
+
+import gc
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import bench  # noqa: E402
+from oracle import plan as oplan  # noqa: E402
+from oracle import step as ostep  # noqa: E402
+from synth import philox, workloads  # noqa: E402
+from tests import gpu_harness as H  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_plan(w):
+    return oplan.build_partition(w.numel, w.n_ranks, threshold=w.persistence_threshold,
+                                 reduce_bucket_size=w.reduce_bucket_size,
+                                 prefetch_bucket_size=w.prefetch_bucket_size,
+                                 sub_group_size=w.sub_group_size, ds_id=w.ds_id)
+
+
+def _samples(op, rng, n_random=3000):
+    """(rank, column) of random shard elements plus the first, last,
+    padding and alignment columns of 40 random partitioned parameters."""
+    N, S = op.n_ranks, op.S
+    rs = list(rng.integers(0, N, size=n_random))
+    cs = list(rng.integers(0, S, size=n_random))
+    part = [p for p in op.params if not p.persistent and p.ps > 0]
+    for p in rng.permutation(len(part))[:40]:
+        p = part[p]
+        for r in (0, N // 2, N - 1):
+            for j in (0, p.ps - 1, p.ps // 2, min(p.ps + 3, (p.ps + 7) // 8 * 8 - 1)):
+                if 0 <= j < (p.ps + 7) // 8 * 8:
+                    rs.append(r)
+                    cs.append(p.shard_off + j)
+    return np.array(rs, dtype=np.int64), np.array(cs, dtype=np.int64)
+
+
+def _locate(op, w, dw, cols, ranks):
+    """For each sampled element: kind (0 data, 1 padding/alignment), its
+    parameter element index e, input index and the N pool indices of its
+    rank gradients."""
+    part = sorted([p for p in op.params if not p.persistent and p.ps > 0], key=lambda p: p.shard_off)
+    starts = np.array([p.shard_off for p in part], dtype=np.int64)
+    pi = np.searchsorted(starts, cols, side="right") - 1
+    N = op.n_ranks
+    kind = np.ones(len(cols), dtype=np.int64)
+    win = np.zeros(len(cols), dtype=np.int64)
+    pool_idx = np.zeros((N, len(cols)), dtype=np.uint64)
+    for s, (c, r, k) in enumerate(zip(cols, ranks, pi)):
+        p = part[k]
+        j = int(c) - p.shard_off
+        if j >= p.ps:
+            continue
+        e = int(r) * p.ps + j
+        if e >= p.numel:
+            continue
+        for b in p.reduce_buckets:
+            ent = [x for x in op.reduce_buckets[b] if x.param == p.index][0]
+            if ent.e_lo <= e < ent.e_hi:
+                pos = ent.buf_off + e - ent.e_lo
+                pool_idx[:, s] = [dw.offs[b][q] + pos for q in range(N)]
+                break
+        kind[s] = 0
+        win[s] = p.input_off + e
+    return kind, win, pool_idx
+
+
+@pytest.mark.parametrize("name", ["llama_layer", "many_small", "llama3_16_layers", "llama3_8b"])
+def test_fullsize_sampled(name):
+    w = workloads.WORKLOADS[name]()
+    op = _oracle_plan(w)
+    dw = bench.DeviceWorkload(w, "cuda:0", max_norm=0.0)
+    try:
+        assert dw.info["shard_elems"] == op.S and dw.info["flat_elems"] == op.flat_elems
+        dw.step()
+        torch.cuda.synchronize()
+        assert int(dw.d_flags[0]) == 0 and float(dw.d_coef[0]) == 1.0
+        rng = np.random.default_rng(11)
+        ranks, cols = _samples(op, rng)
+        idx = torch.from_numpy(ranks * op.S + cols).to(dw.dev)
+        got = {k: getattr(dw, a).index_select(0, idx).cpu().numpy()
+               for k, a in [("gs", "gs"), ("ps", "ps"), ("p", "master"), ("m", "m"), ("v", "v")]}
+        kind, win, pidx = _locate(op, w, dw, cols, ranks)
+        data = kind == 0
+        vals = philox.grad_bf16(w.seed, 0, pidx[:, data].ravel(), w.grad_sigma, w.outlier_frac,
+                                w.outlier_scale).reshape(op.n_ranks, -1)
+        gs_ref = ostep.reduce_mean_bf16(vals)
+        W = philox.weight_f32(w.seed, win[data].astype(np.uint64), w.weight_sigma)
+        z = np.zeros_like(W)
+        p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, np.float32(1.0),
+                                           ostep.adam_consts(w.hparams(), 1))
+        assert np.array_equal(got["gs"].view(np.uint16)[data], gs_ref)
+        H.assert_f32_close(got["p"][data], p1, "master")
+        H.assert_f32_close(got["m"][data], m1, "exp_avg")
+        H.assert_f32_close(got["v"][data], v1, "exp_avg_sq")
+        H.assert_bf16_within_ulp(got["ps"].view(np.uint16)[data], pb, "param_shards")
+        # padding and alignment columns stay exactly zero
+        for k in ("gs", "ps", "p", "m", "v"):
+            assert not np.any(got[k].view(np.uint8).reshape(len(cols), -1)[~data])
+        # gathered parameters: the bf16 shard values at their flat positions
+        part = sorted([p for p in op.params if not p.persistent and p.ps > 0],
+                      key=lambda p: p.shard_off)
+        starts = np.array([p.shard_off for p in part])
+        fpos, fsrc = [], []
+        for s in np.nonzero(data)[0]:
+            p = part[np.searchsorted(starts, cols[s], side="right") - 1]
+            fpos.append(p.flat_off + int(ranks[s]) * p.ps + int(cols[s]) - p.shard_off)
+            fsrc.append(s)
+        fl = dw.flat.index_select(0, torch.tensor(fpos, device=dw.dev)).cpu().numpy()
+        assert np.array_equal(fl.view(np.uint16), got["ps"].view(np.uint16)[fsrc])
+        # persistent parameters: sampled elements
+        pers = [p for p in op.params if p.persistent and p.numel > 0]
+        if pers:
+            P = pers[:: max(1, len(pers) // 30)]
+            ents = []
+            for p in P:
+                for e in sorted(set([0, p.numel - 1, p.numel // 3])):
+                    b = p.reduce_buckets[0]
+                    ent = [x for x in op.reduce_buckets[b] if x.param == p.index][0]
+                    ents.append((p.persist_off + e, p.input_off + e,
+                                 [dw.offs[b][q] + ent.buf_off + e for q in range(op.n_ranks)]))
+            pidx2 = torch.tensor([x[0] for x in ents], device=dw.dev)
+            pv = philox.grad_bf16(w.seed, 0, np.array([x[2] for x in ents], dtype=np.uint64).T.ravel(),
+                                  w.grad_sigma, w.outlier_frac, w.outlier_scale).reshape(op.n_ranks, -1)
+            gP_ref = ostep.reduce_mean_bf16(pv)
+            assert np.array_equal(dw.gP.index_select(0, pidx2).cpu().numpy().view(np.uint16), gP_ref)
+            Wp = philox.weight_f32(w.seed, np.array([x[1] for x in ents], dtype=np.uint64),
+                                   w.weight_sigma)
+            zp = np.zeros_like(Wp)
+            pp1 = ostep.adam_update(Wp, zp, zp, gP_ref, np.float32(1.0),
+                                    ostep.adam_consts(w.hparams(), 1))[0]
+            H.assert_f32_close(dw.pm.index_select(0, pidx2).cpu().numpy(), pp1, "p_master")
+        # the norm is the norm of the reduced-gradient buffers
+        tot = 0.0
+        for buf, n in ((dw.gs, op.n_ranks * op.S), (dw.gP, op.Pn_alloc)):
+            for ch in buf[:n].split(1 << 27):
+                x = ch.view(torch.bfloat16).double()
+                tot += float((x * x).sum())
+        ref = float(np.sqrt(tot))
+        assert abs(float(dw.d_norm[0]) - ref) <= 1e-5 * ref
+    finally:
+        del dw
+        gc.collect()
+        torch.cuda.empty_cache()

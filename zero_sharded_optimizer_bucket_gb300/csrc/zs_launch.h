@@ -1,0 +1,55 @@
+// Host-side launchers of the libzs kernels (called by the C ABI in zs_api.cu
+// after argument checks).  Each returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zs_internal.h"
+
+struct ZsAdamScalars {
+    float lr, b1, b2, omb1, omb2, eps, wd, lr_wd, bc1, bc2;
+    int adamw;
+};
+
+cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+                               const void *const *rank_ptrs, int N, uint16_t *gs, uint16_t *gP,
+                               double *partials, cudaStream_t s);
+
+cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
+                                   const void *const *d_table, int N, uint16_t *gs, uint16_t *gP,
+                                   double *partials, cudaStream_t s);
+
+cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, const uint16_t *gs,
+                     const uint16_t *gP, double *scratch, bool recompute, float max_norm,
+                     float *d_norm, float *d_coef, int32_t *d_flags, cudaStream_t s);
+
+cudaError_t zsl_adam(int N, int64_t S, int64_t s_lo, int64_t s_hi, int64_t p_lo, int64_t p_hi,
+                     const ZsAdamScalars &c, const float *d_coef, const int32_t *d_flags,
+                     const zs_shard_state &st, cudaStream_t s);
+
+cudaError_t zsl_step2(const ZsTile *d_tiles, int64_t ntiles, const ZsAdamScalars &c,
+                      const float *d_coef, const int32_t *d_flags, const zs_shard_state &st,
+                      uint16_t *flat_out, cudaStream_t s);
+
+cudaError_t zsl_partition(const ZsTile *d_tiles, int64_t ntiles, const float *W,
+                          const zs_shard_state &st, cudaStream_t s);
+
+// One gather launch covers the output range [out_lo, out_hi) of flat_out,
+// made of at most ZS_GATHER_MAX parameters laid out back to back.
+constexpr int ZS_GATHER_MAX = 128;   // keeps the launch arguments under 4 KB
+struct ZsGatherEntry {
+    int64_t out_off;    // first element of the parameter in flat_out
+    int64_t shard_off;  // S_p
+    int64_t ps;         // > 0
+};
+struct ZsGatherArgs {
+    ZsGatherEntry e[ZS_GATHER_MAX];
+    int32_t n;
+    int32_t N;
+    int64_t S;
+    int64_t out_lo, out_hi;
+};
+
+cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
+                       cudaStream_t s);
