@@ -268,6 +268,35 @@ zs_status zs_grad_norm(const zs_plan *plan, const void *grad_shards, const void 
                        double *norm_scratch, int32_t recompute, float max_norm, float *d_norm,
                        float *d_clip_coef, int32_t *d_flags, void *stream);
 
+/* Size, in doubles, of the norm scratch array built into the library for
+ * zs_grad_norm_noalloc (8 MiB of device memory per GPU that loads it). */
+#define ZS_NOALLOC_NORM_MAX_SCRATCH (1LL << 20)
+
+/* zs_grad_norm with recompute = 1, for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this exists for callers that are
+ * handed only their inputs and outputs (a plugin inside a host framework
+ * that owns every device allocation) or that must keep cudaMalloc, which
+ * can synchronise the device, out of their step loop.  The scratch lives in
+ * an array of ZS_NOALLOC_NORM_MAX_SCRATCH doubles inside the library;
+ * nothing is allocated.  Same inputs and outputs as zs_grad_norm (the
+ * reduced gradients, max_norm, device scalars d_norm, d_clip_coef,
+ * d_flags); the result equals zs_grad_norm(..., recompute = 1, ...) bit for
+ * bit.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ * - Every call on a device shares the one array and it keeps the last
+ *   call's contents; each call writes every element it reads, so nothing
+ *   needs clearing.  Calls that overlap on the GPU (other streams, other
+ *   host threads) race on the array and give wrong norms.
+ * - Errors: ZS_EINVAL when the plan needs more than
+ *   ZS_NOALLOC_NORM_MAX_SCRATCH doubles (n_tiles + first-level blocks, i.e.
+ *   about 8.6e9 elements) or on a bad pointer, ZS_ESTATE when the plan is
+ *   not uploaded, ZS_ECUDA. */
+zs_status zs_grad_norm_noalloc(const zs_plan *plan, const void *grad_shards,
+                               const void *persist_grads, float max_norm, float *d_norm,
+                               float *d_clip_coef, int32_t *d_flags, void *stream);
+
 /* A4 — Adam(W) on one sub-group (-1: all) of every rank's fp32 shard and
  * of its persistent parameters, then the bf16 cast of the new master into
  * param_shards / persist_params ([ZeRO-3 chapter] §6.3: per sub-group

@@ -27,6 +27,7 @@ _lib = C.CDLL(LIB_PATH)
 ZS_OK, ZS_EINVAL, ZS_ENOMEM, ZS_ECUDA, ZS_ESTATE, ZS_ETIMEOUT = 0, -1, -2, -3, -4, -5
 ZS_MAX_RANKS = 256
 ZS_SKIP_NONFINITE = 1
+ZS_NOALLOC_NORM_MAX_SCRATCH = 1 << 20
 TILE_DTYPE = [("dst", "<i8"), ("src", "<i8"), ("flat", "<i8"), ("win", "<i8"),
               ("len", "<i4"), ("valid", "<i4"), ("flat_len", "<i4"), ("bucket", "<i4")]
 
@@ -125,6 +126,7 @@ _sig("zs_all_gather_coalesced", _i32, [_P, _i32, C.POINTER(_i32), _P, _P, _i64, 
 _sig("zs_reduce_scatter_all", _i32, [_P, _P, _P, _P, _P, _P])
 _sig("zs_adam_gather", _i32, [_P, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                               C.POINTER(zs_shard_state), _P, _P])
+_sig("zs_grad_norm_noalloc", _i32, [_P, _P, _P, _f32, _P, _P, _P, _P])
 _sig("zs_shard_step", _i32, [_P, _P, C.POINTER(zs_shard_state), _P, C.POINTER(zs_adam_hparams),
                              _i64, _f32, _P, _P, _P, _P, _P])
 
@@ -365,3 +367,12 @@ def zs_adam_gather(plan, hp, step: int, d_clip_coef, d_flags, state: zs_shard_st
     h = _hp(hp)
     _check(_lib.zs_adam_gather(_h(plan), C.byref(h), int(step), _ptr(d_clip_coef), _ptr(d_flags),
                                C.byref(state), _ptr(flat_out), _stream(stream)), "zs_adam_gather")
+
+
+def zs_grad_norm_noalloc(plan, grad_shards, persist_grads, max_norm: float, d_norm, d_clip_coef,
+                         d_flags, stream=None) -> None:
+    """zs_grad_norm(recompute=1) with the library's built-in scratch array,
+    for callers that cannot allocate device memory."""
+    _check(_lib.zs_grad_norm_noalloc(_h(plan), _ptr(grad_shards), _ptr(persist_grads),
+                                     float(max_norm), _ptr(d_norm), _ptr(d_clip_coef),
+                                     _ptr(d_flags), _stream(stream)), "zs_grad_norm_noalloc")
