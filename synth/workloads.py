@@ -154,12 +154,23 @@ def llama3_8b() -> Workload:
                     max_norm=1.0, seed=0x5EED0005)
 
 
+def llama3_attn() -> Workload:
+    """One attention block of the Llama-3-8B shapes (q, k, v, o and the input
+    norm, 41.9M elements), N=16: the small case for detailed profiles (a
+    reduce-scatter launch still reads 1.3 GB, ten times the L2)."""
+    n, s = _llama_layer(4096, 14336, 1024, "layers.0")
+    keep = [0, 1, 2, 3, 7]
+    return Workload("llama3_attn", 16, [n[i] for i in keep], [s[i] for i in keep],
+                    grad_sigma=1e-3, steps=1, max_norm=1.0, seed=0x5EED0006)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama_layer": llama_layer,
     "many_small": many_small,
     "llama3_16_layers": llama3_layers,
     "llama3_8b": llama3_8b,
+    "llama3_attn": llama3_attn,
 }
 
 
