@@ -7,7 +7,9 @@
 // load when source and destination have the same phase, else two aligned
 // loads and a lane shift), adds them to 8 float32 sums, then writes
 // bf16_rne(sum / N).  The rank loop is sequential per element, so the
-// result is bit-exact against the fixed-order definition.
+// result is bit-exact against the fixed-order definition.  Five CTAs of 256
+// threads per SM (registers capped by the launch bounds) keep enough loads
+// in flight to stream the N gradient buffers near the HBM read bandwidth.
 #include "zs_device.cuh"
 #include "zs_launch.h"
 
@@ -18,7 +20,7 @@ struct RankPtrs {
 };
 
 template <bool FROM_TABLE>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 5)
 rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
           const uint16_t *const *__restrict__ table, int N, float fN,
           uint16_t *__restrict__ gs, uint16_t *__restrict__ gP, double *__restrict__ partials) {
@@ -47,6 +49,11 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     const int64_t delta = tile.src - D;
     const int q = (int)((G0 + delta) & 7);
     const int64_t vs = tile.src, ve = tile.src + tile.valid;
+    // For N a power of two, 1/N is exact and s * (1/N) is the same single
+    // rounding of the exact quotient as s / N, bit for bit; the multiply is
+    // far cheaper than an IEEE division.  Other N divide.
+    const bool pow2 = (N & (N - 1)) == 0;
+    const float invN = 1.0f / fN;
     float sq32 = 0.0f;
     double sq64 = 0.0;
     for (int64_t gi = threadIdx.x; gi < ngroups; gi += THREADS) {
@@ -80,7 +87,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         }
         uint32_t r[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = f2bf(__fdiv_rn(acc[i], fN));
+        for (int i = 0; i < 8; ++i) r[i] = f2bf(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN));
         group_sq(r, sq32, sq64);
         if (x0 >= D && x0 + 8 <= D + tile.len) {
             *reinterpret_cast<uint4 *>(out + x0) = pack8(r);
