@@ -146,6 +146,33 @@ class DeviceWorkload:
                           self.flat)
         ev[3].record()
 
+    def unfused_step(self):
+        """The same step through the per-call API: zs_reduce_scatter per
+        bucket, zs_grad_norm, zs_adam_step per sub-group, then
+        zs_all_gather_coalesced per gather bucket into its place in model
+        flat space.  Returns the number of kernel launches it made."""
+        zs = self.zs
+        if not hasattr(self, "_gathers"):
+            self._bptrs = [self.bucket_ptrs(b) for b in range(len(self.buf_elems))]
+            self._gathers = []
+            for g in range(self.info["n_gather_buckets"]):
+                gi = zs.zs_gather_bucket_info(self.plan, g)
+                ps = [zs.zs_gather_bucket_param(self.plan, g, i) for i in range(gi["n_params"])]
+                self._gathers.append((ps, self.flat.data_ptr() + 2 * gi["flat_offset"],
+                                      gi["flat_elems"]))
+        self.t += 1
+        for b, ptrs in enumerate(self._bptrs):
+            zs.zs_reduce_scatter(self.plan, b, ptrs, self.gs, self.gP, self.scratch)
+        zs.zs_grad_norm(self.plan, self.gs, self.gP, self.scratch, False, self.max_norm,
+                        self.d_norm, self.d_coef, self.d_flags)
+        for sg in range(self.info["n_sub_groups"]):
+            zs.zs_adam_step(self.plan, sg, self.hp, self.t, self.d_coef, self.d_flags, self.state)
+        launches = len(self._bptrs) + 2 + self.info["n_sub_groups"]
+        for ps, base, n in self._gathers:
+            zs.zs_all_gather_coalesced(self.plan, ps, self.ps, base, n)
+            launches += (len(ps) + 127) // 128
+        return launches
+
     def algorithmic_bytes(self):
         """Bytes the method must move per step (padding excluded):
         reduce-scatter 2N + 2 per element; Adam + cast 28 per element plus
@@ -448,7 +475,8 @@ def run_gpu(args):
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "storage": "bf16 gradients and parameters, f32 master / exp_avg / exp_avg_sq",
         "data": "synthetic (Philox4x32-10 gradients and weights; architecture shapes only)",
         "config": {"workload": w.name, "n_ranks": w.n_ranks, "psi": psi,
                    "n_params": w.n_params, "reduce_bucket_size": w.reduce_bucket_size,
@@ -469,6 +497,20 @@ def run_gpu(args):
         "clocks": ck,
         "skip_flags": flags,
     }
+    # the same step through the per-call API, for comparison (not the value)
+    dw.unfused_step()
+    torch.cuda.synchronize(dev)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KU = max(2, K // 2)
+    u0.record()
+    for _ in range(KU):
+        n_unfused = dw.unfused_step()
+    u1.record()
+    torch.cuda.synchronize(dev)
+    res["unfused"] = {"ms_per_step": u0.elapsed_time(u1) / KU, "steps": KU,
+                      "launches_per_step": n_unfused,
+                      "calls": "zs_reduce_scatter per bucket, zs_grad_norm, zs_adam_step per "
+                               "sub-group, zs_all_gather_coalesced per gather bucket"}
     if not args.no_e2e:
         res["e2e"] = run_e2e(dw, steps=args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -184,9 +184,11 @@ def pool_offsets(bucket_buf_elems, n_ranks: int, pool_elems: int):
     """
     offs = []
     run = 0
+    total = sum((int(L) + 7) // 8 * 8 for L in bucket_buf_elems) * n_ranks
+    wraps = total > pool_elems
     for L in bucket_buf_elems:
         L8 = (int(L) + 7) // 8 * 8
-        if L8 * (n_ranks + 1) > pool_elems:
+        if wraps and L8 * (n_ranks + 1) > pool_elems:
             # (N+1) buffers guarantee that the buffers of one bucket never
             # overlap when the layout wraps around in the middle of a bucket
             raise ValueError("gradient pool smaller than N+1 buffers of one bucket")

@@ -49,3 +49,8 @@ def test_pool_offsets_disjoint_within_bucket():
         for (a, b), (c, d) in zip(spans, spans[1:]):
             assert b <= c
         assert all(o % 8 == 0 and o + L <= 30_000 for o in row)
+
+
+def test_pool_offsets_exact_fit_without_wrap():
+    offs = workloads.pool_offsets([40], 4, 160)
+    assert offs == [[0, 40, 80, 120]]
