@@ -1,12 +1,12 @@
 // A2 reduce-scatter (with the A3 partial sums) and the A3 norm kernels.
 //
 // Reduce-scatter ([ZeRO-3 chapter] §6.2, avg-scatter of a full bucket):
-// one CTA per tile.  A thread owns 8-element groups of destination slots
-// aligned to 16 bytes in shard space; for each rank k in order 0..N-1 it
-// loads the matching 8 gradients of rank k's bucket buffer (one 16-byte
-// load when source and destination have the same phase, else two aligned
-// loads and a lane shift), adds them to 8 float32 sums, then writes
-// bf16_rne(sum / N).  The rank loop is sequential per element, so the
+// one CTA per tile.  A thread owns 8-element chunks aligned to 16 bytes in
+// the rank buffers; for each rank k in order 0..N-1 it loads the chunk of
+// rank k's bucket buffer with one 16-byte load, adds the 8 values to 8
+// float32 sums, then writes bf16_rne(sum / N) to the owners' shard slots
+// (one 16-byte store; when shard and bucket have different phases the
+// results are realigned once across neighbouring lanes).  The rank loop is sequential per element, so the
 // result is bit-exact against the fixed-order definition.  Five CTAs of 256
 // threads per SM (registers capped by the launch bounds) keep enough loads
 // in flight to stream the N gradient buffers near the HBM read bandwidth.
@@ -44,11 +44,19 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         return;
     }
     uint16_t *__restrict__ out = tile.flat < 0 ? gP : gs;
-    const int64_t D = tile.dst, G0 = D & ~int64_t(7);
-    const int64_t ngroups = (D + tile.len - G0 + 7) >> 3;
+    const int64_t D = tile.dst, V = tile.valid;
     const int64_t delta = tile.src - D;
-    const int q = (int)((G0 + delta) & 7);
-    const int64_t vs = tile.src, ve = tile.src + tile.valid;
+    const int64_t vs = tile.src, ve = tile.src + V;
+    // Work goes by 8-element chunks aligned in the SOURCE (the rank buffers):
+    // one plain 16-byte load per rank and chunk.  The 8 results of a chunk
+    // land at destination offset a = (-delta) mod 8 within an aligned group;
+    // when a != 0 they are realigned once, after the rank loop: a lane's
+    // last a results and the next lane's first 8-a results form one aligned
+    // destination group (warp shuffle), stored as one 16-byte vector.
+    const int a = (int)((-delta) & 7);
+    const int64_t c_first = vs >> 3;
+    const int64_t nchunks = V > 0 ? ((ve - 1) >> 3) - c_first + 1 : 0;
+    const int lane = threadIdx.x & 31;
     // For N a power of two, 1/N is exact and s * (1/N) is the same single
     // rounding of the exact quotient as s / N, bit for bit; the multiply is
     // far cheaper than an IEEE division.  Other N divide.
@@ -56,45 +64,81 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     const float invN = 1.0f / fN;
     float sq32 = 0.0f;
     double sq64 = 0.0;
-    for (int64_t gi = threadIdx.x; gi < ngroups; gi += THREADS) {
-        const int64_t x0 = G0 + 8 * gi;
-        const int64_t s0 = x0 + delta;
-        const int64_t c0 = s0 >> 3;  // floor
-        const int64_t lo = vs - s0, hi = ve - s0;
+    // uniform trip count: every lane takes part in the shuffles
+    for (int64_t base = 0; base < nchunks; base += THREADS) {
+        const int64_t gi = base + threadIdx.x;
+        const bool act = gi < nchunks;
+        const int64_t c = c_first + gi;
+        const int64_t lo = vs - 8 * c, hi = ve - 8 * c;  // valid lanes [lo, hi)
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        if (q == 0 && lo <= 0 && hi >= 8) {
-            const int64_t off = 8 * c0;
+        if (act) {
+            const uint16_t *const *__restrict__ p = sp;
+            if (lo <= 0 && hi >= 8) {
 #pragma unroll 8
-            for (int k = 0; k < N; ++k) {
-                const uint4 v = ldg16(sp[k] + off);
+                for (int k = 0; k < N; ++k) {
+                    const uint4 v = ldg16(p[k] + 8 * c);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], bf2f(lane16(v, i)));
-            }
-        } else {
-            const bool ld0 = (8 * c0 + 8 > vs) && (8 * c0 < ve);
-            const bool ld1 = q != 0 && (8 * c0 + 16 > vs) && (8 * c0 + 8 < ve);
+                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], bf2f(lane16(v, i)));
+                }
+            } else {
 #pragma unroll 4
-            for (int k = 0; k < N; ++k) {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                const uint4 a = ld0 ? ldg16(sp[k] + 8 * c0) : z;
-                const uint4 b = ld1 ? ldg16(sp[k] + 8 * c0 + 8) : z;
-                const uint4 v = mask8(shift8(a, b, q), lo, hi);
+                for (int k = 0; k < N; ++k) {
+                    const uint4 v = mask8(ldg16(p[k] + 8 * c), lo, hi);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], bf2f(lane16(v, i)));
+                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], bf2f(lane16(v, i)));
+                }
             }
         }
         uint32_t r[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = f2bf(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN));
-        group_sq(r, sq32, sq64);
-        if (x0 >= D && x0 + 8 <= D + tile.len) {
-            *reinterpret_cast<uint4 *>(out + x0) = pack8(r);
+        for (int i = 0; i < 8; ++i)
+            r[i] = act ? f2bf(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN)) : 0u;
+        if (act) group_sq(r, sq32, sq64);
+        const int64_t y0 = 8 * c - delta;  // destination of lane 0 of the chunk
+        if (a == 0) {
+            if (act) {
+                if (lo <= 0 && hi >= 8) {
+                    *reinterpret_cast<uint4 *>(out + y0) = pack8(r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i >= lo && i < hi) out[y0 + i] = (uint16_t)r[i];
+                }
+            }
+        } else {
+            const uint4 w = pack8(r);
+            uint4 wn;
+            wn.x = __shfl_down_sync(0xFFFFFFFFu, w.x, 1);
+            wn.y = __shfl_down_sync(0xFFFFFFFFu, w.y, 1);
+            wn.z = __shfl_down_sync(0xFFFFFFFFu, w.z, 1);
+            wn.w = __shfl_down_sync(0xFFFFFFFFu, w.w, 1);
+            const bool next_act = __shfl_down_sync(0xFFFFFFFFu, (int)act, 1) != 0 && lane < 31;
+            // my lanes [8-a, 8) and the next chunk's lanes [0, 8-a) all valid
+            const bool vec = act && next_act && lo <= 8 - a && hi >= 16 - a;
+            if (vec) *reinterpret_cast<uint4 *>(out + y0 + 8 - a) = shift8(w, wn, 8 - a);
+            const bool prev_vec = __shfl_up_sync(0xFFFFFFFFu, (int)vec, 1) != 0 && lane > 0;
+            if (act) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const bool head = i < 8 - a;  // stored by the previous lane's vector?
+                    const bool done = head ? prev_vec : vec;
+                    if (!done && i >= lo && i < hi) out[y0 + i] = (uint16_t)r[i];
+                }
+            }
+        }
+    }
+    // padding of the tile (beyond the valid prefix): zeros
+    const int64_t p0 = D + V, p1 = D + tile.len;
+    for (int64_t g = (p0 >> 3) + threadIdx.x; g <= ((p1 - 1) >> 3) && p1 > p0; g += THREADS) {
+        const int64_t x0 = 8 * g;
+        if (x0 >= p0 && x0 + 8 <= p1) {
+            *reinterpret_cast<uint4 *>(out + x0) = make_uint4(0, 0, 0, 0);
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                if (x0 + i >= D && x0 + i < D + tile.len) out[x0 + i] = (uint16_t)r[i];
+                if (x0 + i >= p0 && x0 + i < p1) out[x0 + i] = 0;
         }
     }
     if (partials) {
@@ -103,8 +147,9 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     }
 }
 
-// Recompute the per-tile partial sums from the reduced gradients; the same
-// group and thread mapping as rs_kernel, so the same bits.
+// Recompute the per-tile partial sums from the reduced gradients, with
+// the chunks and the thread mapping of rs_kernel (8-element chunks aligned in
+// the source, chunk gi on thread gi mod THREADS), so the same bits.
 __global__ void __launch_bounds__(THREADS)
 norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__ gs,
                   const uint16_t *__restrict__ gP, double *__restrict__ partials) {
@@ -112,16 +157,27 @@ norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__
     const int64_t t = blockIdx.x;
     const ZsTile tile = tiles[t];
     const uint16_t *__restrict__ in = tile.flat < 0 ? gP : gs;
-    const int64_t D = tile.dst, G0 = D & ~int64_t(7);
-    const int64_t ngroups = (D + tile.len - G0 + 7) >> 3;
+    const int64_t D = tile.dst, V = tile.valid;
+    const int64_t delta = tile.src - D;
+    const int64_t vs = tile.src, ve = tile.src + V;
+    const int a = (int)((-delta) & 7);
+    const int64_t c_first = vs >> 3;
+    const int64_t nchunks = V > 0 ? ((ve - 1) >> 3) - c_first + 1 : 0;
     float sq32 = 0.0f;
     double sq64 = 0.0;
-    for (int64_t gi = threadIdx.x; gi < ngroups; gi += THREADS) {
-        const int64_t x0 = G0 + 8 * gi;
-        const uint4 v = mask8(ldg16(in + x0), D - x0, D + tile.len - x0);
+    for (int64_t gi = threadIdx.x; gi < nchunks; gi += THREADS) {
+        const int64_t c = c_first + gi;
+        const int64_t lo = vs - 8 * c, hi = ve - 8 * c;
+        const int64_t y0 = 8 * c - delta;
         uint32_t r[8];
+        if (a == 0 && lo <= 0 && hi >= 8) {
+            const uint4 v = ldg16(in + y0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = lane16(v, i);
+            for (int i = 0; i < 8; ++i) r[i] = lane16(v, i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r[i] = (i >= lo && i < hi) ? (uint32_t)in[y0 + i] : 0u;
+        }
         group_sq(r, sq32, sq64);
     }
     const double s = block_sum(__dadd_rn((double)sq32, sq64), red);
