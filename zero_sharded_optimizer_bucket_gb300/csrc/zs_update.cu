@@ -112,25 +112,59 @@ step2_kernel(const ZsTile *__restrict__ tiles, AdamC c, const float *__restrict_
     const int64_t ngroups = (D + L - G0 + 7) >> 3;
     const int64_t fdelta = tile.flat - D;
     const int fq = (int)((a0 + G0 + fdelta) & 7);
-    for (int64_t gi = threadIdx.x; gi < ngroups; gi += THREADS) {
+    const int lane = threadIdx.x & 31;
+    // uniform trip count: every lane takes part in the shuffles below
+    for (int64_t base = 0; base < ngroups; base += THREADS) {
+        const int64_t gi = base + threadIdx.x;
+        const bool act = gi < ngroups;
         const int64_t x0 = G0 + 8 * gi;
         uint32_t r[8];
-        if (x0 >= D && x0 + 8 <= D + L) {
-            adam8(s, x0, coef, c, r);
-        } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                r[i] = (x0 + i >= D && x0 + i < D + L) ? adam1(s, x0 + i, coef, c) : 0u;
-        }
-        if (!pers) {
-            const int64_t li0 = x0 - D;
-            if (fq == 0 && li0 >= 0 && li0 + 8 <= tile.flat_len) {
-                *reinterpret_cast<uint4 *>(flat_out + x0 + fdelta) = pack8(r);
+        for (int i = 0; i < 8; ++i) r[i] = 0u;
+        if (act) {
+            if (x0 >= D && x0 + 8 <= D + L) {
+                adam8(s, x0, coef, c, r);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (li0 + i >= 0 && li0 + i < tile.flat_len)
-                        flat_out[x0 + i + fdelta] = (uint16_t)r[i];
+                    if (x0 + i >= D && x0 + i < D + L) r[i] = adam1(s, x0 + i, coef, c);
+            }
+        }
+        if (pers) continue;
+        // slots i with li0 + i in [0, flat_len) go to model flat space
+        const int64_t li0 = x0 - D;
+        const int64_t lo = -li0, hi = tile.flat_len - li0;
+        if (fq == 0) {
+            if (act) {
+                if (lo <= 0 && hi >= 8) {
+                    *reinterpret_cast<uint4 *>(flat_out + x0 + fdelta) = pack8(r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i >= lo && i < hi) flat_out[x0 + i + fdelta] = (uint16_t)r[i];
+                }
+            }
+        } else {
+            // the group's flat positions start fq past a 16-byte boundary:
+            // slots [8-fq, 8) of this lane and [0, 8-fq) of the next lane
+            // make one aligned 16-byte store
+            const uint4 w = pack8(r);
+            uint4 wn;
+            wn.x = __shfl_down_sync(0xFFFFFFFFu, w.x, 1);
+            wn.y = __shfl_down_sync(0xFFFFFFFFu, w.y, 1);
+            wn.z = __shfl_down_sync(0xFFFFFFFFu, w.z, 1);
+            wn.w = __shfl_down_sync(0xFFFFFFFFu, w.w, 1);
+            const bool next_act = __shfl_down_sync(0xFFFFFFFFu, (int)act, 1) != 0 && lane < 31;
+            const bool vec = act && next_act && lo <= 8 - fq && hi >= 16 - fq;
+            if (vec)
+                *reinterpret_cast<uint4 *>(flat_out + x0 + fdelta + 8 - fq) = shift8(w, wn, 8 - fq);
+            const bool prev_vec = __shfl_up_sync(0xFFFFFFFFu, (int)vec, 1) != 0 && lane > 0;
+            if (act) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const bool done = (i < 8 - fq) ? prev_vec : vec;
+                    if (!done && i >= lo && i < hi) flat_out[x0 + i + fdelta] = (uint16_t)r[i];
+                }
             }
         }
     }
