@@ -97,6 +97,7 @@ class GatherBucket:
 @dataclass
 class Plan:
     n_ranks: int
+    dtype: str              # 16-bit storage of gradients and parameters: "bf16" | "fp16"
     threshold: int
     reduce_bucket_size: int
     prefetch_bucket_size: int
@@ -128,7 +129,8 @@ class Plan:
 def build_partition(numel, n_ranks: int, threshold: int = 100_000,
                     reduce_bucket_size: int = 5_000_000,
                     prefetch_bucket_size: int = 50_000_000,
-                    sub_group_size: int = 1_000_000_000, ds_id=None) -> Plan:
+                    sub_group_size: int = 1_000_000_000, ds_id=None,
+                    dtype: str = "bf16") -> Plan:
     numel = [int(x) for x in numel]
     n = len(numel)
     if n_ranks < 1:
@@ -137,6 +139,8 @@ def build_partition(numel, n_ranks: int, threshold: int = 100_000,
         raise ValueError("bucket and sub-group sizes must be >= 1")
     if any(x < 0 for x in numel):
         raise ValueError("numel must be >= 0")
+    if dtype not in ("bf16", "fp16"):
+        raise ValueError("dtype must be bf16 or fp16")
     if ds_id is None:
         ds_id = list(range(n))
     ds_id = [int(x) for x in ds_id]
@@ -247,7 +251,7 @@ def build_partition(numel, n_ranks: int, threshold: int = 100_000,
                 s_cur = p.shard_off + _align8(p.ps)
         sub_groups.append(SubGroup(ids, s_lo, s_cur, p_lo, p_cur))
 
-    return Plan(n_ranks=N, threshold=threshold, reduce_bucket_size=B,
+    return Plan(n_ranks=N, dtype=dtype, threshold=threshold, reduce_bucket_size=B,
                 prefetch_bucket_size=G, sub_group_size=U, params=params,
                 order=order, S=s_run, S_logical=S_logical, Pn_alloc=p_run, Pn=Pn,
                 psi=sum(numel), flat_elems=f_run, input_elems=w_run,

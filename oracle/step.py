@@ -4,7 +4,8 @@ A5 all_gather_coalesced: the oracle's arithmetic.
 Floating point is numpy float32, one IEEE operation per step below, in the
 order written; the gradient norm is float64 with an exactly rounded sum
 (math.fsum).  Buffers are numpy arrays in the layouts of `oracle.plan`:
-    grad_shards, param_shards  uint16  [N][S]   (bfloat16 bit patterns)
+    grad_shards, param_shards  uint16  [N][S]   (bfloat16 or, when the plan's
+                                                 dtype is fp16, binary16 bits)
     master, exp_avg, exp_avg_sq float32 [N][S]
     persist_* likewise, [Pn_alloc]
 """
@@ -16,7 +17,16 @@ from dataclasses import dataclass
 import numpy as np
 
 from .bf16 import bf16_to_f32, f32_to_bf16
+from .fp16 import f32_to_fp16, fp16_to_f32
 from .plan import Plan
+
+
+def to_f32(u16, dtype: str = "bf16") -> np.ndarray:
+    return bf16_to_f32(u16) if dtype == "bf16" else fp16_to_f32(u16)
+
+
+def from_f32(x, dtype: str = "bf16") -> np.ndarray:
+    return f32_to_bf16(x) if dtype == "bf16" else f32_to_fp16(x)
 
 F32 = np.float32
 
@@ -66,8 +76,8 @@ def partition(plan: Plan, W: np.ndarray) -> State:
         vals = np.zeros(e.shape, dtype=np.float32)
         vals[valid] = W[p.input_off + e[valid]]
         st.master[e // p.ps, p.shard_off + e % p.ps] = vals
-    st.param_shards = f32_to_bf16(st.master)
-    st.persist_params = f32_to_bf16(st.p_master)
+    st.param_shards = from_f32(st.master, plan.dtype)
+    st.persist_params = from_f32(st.p_master, plan.dtype)
     return st
 
 
@@ -85,6 +95,21 @@ def reduce_mean_bf16(vals: np.ndarray) -> np.ndarray:
     return f32_to_bf16(s / F32(N))
 
 
+def reduce_mean_fp16(vals: np.ndarray) -> np.ndarray:
+    """The same mean for fp16 gradients: float32 sum in rank order, s / N,
+    rounded to fp16 (an overflow becomes inf, which the norm then reports)."""
+    vals = np.asarray(vals, dtype=np.uint16)
+    N = vals.shape[0]
+    s = np.zeros(vals.shape[1:], dtype=np.float32)
+    for k in range(N):
+        s = s + fp16_to_f32(vals[k])
+    return f32_to_fp16(s / F32(N))
+
+
+def reduce_mean(vals, dtype: str = "bf16") -> np.ndarray:
+    return reduce_mean_bf16(vals) if dtype == "bf16" else reduce_mean_fp16(vals)
+
+
 def reduce_scatter(plan: Plan, bucket: int, rank_bufs, st: State) -> None:
     """Reduce bucket `bucket` of all N ranks and keep each rank's slice
     ([ZeRO-3 chapter] §6.2: all_reduce of the bucket then each rank keeps its
@@ -98,7 +123,7 @@ def reduce_scatter(plan: Plan, bucket: int, rank_bufs, st: State) -> None:
             L = ent.e_hi - ent.e_lo
             vals = np.stack([np.asarray(b[ent.buf_off:ent.buf_off + L]) for b in rank_bufs])
             st.persist_grads[p.persist_off + ent.e_lo:p.persist_off + ent.e_hi] = \
-                reduce_mean_bf16(vals)
+                reduce_mean(vals, plan.dtype)
             continue
         # the bucket holding the parameter's last element also owns the
         # padding elements numel .. N*ps-1 (gradient zero)
@@ -111,7 +136,7 @@ def reduce_scatter(plan: Plan, bucket: int, rank_bufs, st: State) -> None:
         src = ent.buf_off + (e[valid] - ent.e_lo)
         for k in range(N):
             vals[k, valid] = np.asarray(rank_bufs[k])[src]
-        st.grad_shards[e // p.ps, p.shard_off + e % p.ps] = reduce_mean_bf16(vals)
+        st.grad_shards[e // p.ps, p.shard_off + e % p.ps] = reduce_mean(vals, plan.dtype)
 
 
 # ---------------------------------------------------------------- A3 -----
@@ -125,22 +150,62 @@ def grad_norm(plan: Plan, st: State, max_norm: float):
     silently diverges; [ZeRO-3 chapter] §6.3: unscale_and_clip_grads takes
     global_norm).  norm = float32(sqrt(sum g^2)) with the sum exact in
     float64; coef = min(1, max_norm / (norm + 1e-6)) in float32 (1 when
-    max_norm <= 0); a non-finite norm sets skip (coef reported as 1)."""
-    sq = np.concatenate([bf16_to_f32(st.grad_shards).ravel(),
-                         bf16_to_f32(st.persist_grads).ravel()]).astype(np.float64)
+    max_norm <= 0); a non-finite norm sets skip (coef reported as 1).
+    This is unscale_and_clip with loss scale 1."""
+    return unscale_and_clip(plan, st, max_norm, 1.0)
+
+
+def unscale_and_clip(plan: Plan, st: State, max_norm: float, scale: float):
+    """unscale_and_clip_grads of [ZeRO-3 chapter] §6.3: the stored gradients
+    are the gradients of the loss times `scale` (the loss scale, 1 for bf16).
+    norm = float32(sqrt(sum g^2)) / scale is the norm of the true gradients;
+    clip = min(1, max_norm / (norm + 1e-6)) (1 when max_norm <= 0);
+    coef = clip / scale is the factor the optimizer applies to the stored
+    gradients (float32 operations).  A non-finite norm (an overflow) sets
+    skip, with coef reported as 1."""
+    sq = np.concatenate([to_f32(st.grad_shards, plan.dtype).ravel(),
+                         to_f32(st.persist_grads, plan.dtype).ravel()]).astype(np.float64)
     sq = sq * sq
     if np.all(np.isfinite(sq)):
         total = math.fsum(sq.tolist())
     else:
         total = float(np.sum(sq))
-    norm = F32(np.sqrt(np.float64(total)))
+    S = F32(scale)
+    norm = F32(np.sqrt(np.float64(total))) / S
     skip = not bool(np.isfinite(norm))
-    if skip or max_norm <= 0:
-        coef = F32(1.0)
-    else:
+    if skip:
+        return norm, F32(1.0), True
+    clip = F32(1.0)
+    if max_norm > 0:
         c = F32(max_norm) / (norm + CLIP_EPS)
-        coef = c if c < F32(1.0) else F32(1.0)
-    return norm, coef, skip
+        clip = c if c < F32(1.0) else F32(1.0)
+    return norm, clip / S, False
+
+
+@dataclass
+class LossScaler:
+    """Dynamic loss scale (the scale the caller multiplies the loss by for
+    fp16 gradients).  After a step whose gradients overflowed (skip): scale
+    = max(scale / factor, min_scale) and the count of good steps restarts;
+    after `window` consecutive good steps: scale = scale * factor.  The
+    pages name the unscale step ([ZeRO-3 chapter] §6.3) but not the
+    schedule; this is DeepSpeed's documented dynamic schedule without
+    hysteresis, in float32."""
+    scale: float = 65536.0
+    good: int = 0
+    factor: float = 2.0
+    min_scale: float = 1.0
+    window: int = 1000
+
+    def update(self, overflow: bool) -> None:
+        if overflow:
+            self.scale = float(max(F32(self.scale) / F32(self.factor), F32(self.min_scale)))
+            self.good = 0
+        else:
+            self.good += 1
+            if self.good >= self.window:
+                self.scale = float(F32(self.scale) * F32(self.factor))
+                self.good = 0
 
 
 # ---------------------------------------------------------------- A4 -----
@@ -176,7 +241,7 @@ def adam_consts(hp: dict, step: int) -> AdamConsts:
                       F32(float(lr) * float(wd)), bc1, bc2, bool(hp.get("adamw", 1)))
 
 
-def adam_update(p, m, v, gs_bf16, coef, c: AdamConsts):
+def adam_update(p, m, v, gs_bf16, coef, c: AdamConsts, dtype: str = "bf16"):
     """One Adam(W) update of fp32 master p and moments m, v from the reduced
     bf16 gradient; returns (p, m, v, bf16(p)).  The optimizer sees only the
     rank's fp32 partition ([ZeRO-3 chapter] §6.3) and writes back the 16-bit
@@ -193,7 +258,7 @@ def adam_update(p, m, v, gs_bf16, coef, c: AdamConsts):
     """
     F = lambda a: np.asarray(a, dtype=np.float32)
     p, m, v = F(p), F(m), F(v)
-    g = bf16_to_f32(gs_bf16) * F32(coef)
+    g = to_f32(gs_bf16, dtype) * F32(coef)
     if c.adamw:
         p = p - c.lr_wd * p
     else:
@@ -204,7 +269,7 @@ def adam_update(p, m, v, gs_bf16, coef, c: AdamConsts):
     vh = v / c.bc2
     den = np.sqrt(vh) + c.eps
     p = p - c.lr * (mh / den)
-    return p, m, v, f32_to_bf16(p)
+    return p, m, v, from_f32(p, dtype)
 
 
 def adam_step(plan: Plan, sub_group: int, hp: dict, step: int, coef, skip: bool,
@@ -221,13 +286,15 @@ def adam_step(plan: Plan, sub_group: int, hp: dict, step: int, coef, skip: bool,
         a, b = g.s_lo, g.s_hi
         if b > a:
             p, m, v, pb = adam_update(st.master[:, a:b], st.exp_avg[:, a:b],
-                                      st.exp_avg_sq[:, a:b], st.grad_shards[:, a:b], coef, c)
+                                      st.exp_avg_sq[:, a:b], st.grad_shards[:, a:b], coef, c,
+                                      plan.dtype)
             st.master[:, a:b], st.exp_avg[:, a:b], st.exp_avg_sq[:, a:b] = p, m, v
             st.param_shards[:, a:b] = pb
         a, b = g.p_lo, g.p_hi
         if b > a:
             p, m, v, pb = adam_update(st.p_master[a:b], st.p_exp_avg[a:b],
-                                      st.p_exp_avg_sq[a:b], st.persist_grads[a:b], coef, c)
+                                      st.p_exp_avg_sq[a:b], st.persist_grads[a:b], coef, c,
+                                      plan.dtype)
             st.p_master[a:b], st.p_exp_avg[a:b], st.p_exp_avg_sq[a:b] = p, m, v
             st.persist_params[a:b] = pb
 
@@ -273,13 +340,18 @@ def gather_model(plan: Plan, param_shards: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------------ the step ---
 def shard_step(plan: Plan, st: State, bucket_bufs, hp: dict, step: int,
-               max_norm: float):
+               max_norm: float, scaler: LossScaler = None):
     """One step of the path: reduce-scatter every bucket, global norm and
-    clip coefficient, Adam(W) over every sub-group, then the gathers the
-    next forward pass performs.  bucket_bufs[b][k] is rank k's gradient
+    clip coefficient (unscaled by the loss scale when a scaler is given,
+    which is then updated), Adam(W) over every sub-group, then the gathers
+    the next forward pass performs.  bucket_bufs[b][k] is rank k's gradient
     buffer of bucket b."""
     for b in range(len(plan.reduce_buckets)):
         reduce_scatter(plan, b, bucket_bufs[b], st)
-    norm, coef, skip = grad_norm(plan, st, max_norm)
+    if scaler is None:
+        norm, coef, skip = grad_norm(plan, st, max_norm)
+    else:
+        norm, coef, skip = unscale_and_clip(plan, st, max_norm, scaler.scale)
+        scaler.update(skip)
     adam_step(plan, -1, hp, step, coef, skip, st)
     return norm, coef, skip, gather_model(plan, st.param_shards)

@@ -23,6 +23,9 @@ Value mappings (identical in synth/csrc/synth_gen.cu):
   bf16    : gradients are stored as bfloat16 by keeping the upper 16 bits of
             the float32 value (truncation; a generator convention, chosen so
             that no rounding rule of the method is involved in making inputs).
+  fp16    : fp16 gradients are floor(z / 512) * 2^e (an integer of at most
+            11 bits times a power of two: exactly representable in binary16,
+            so again no rounding is involved); outliers multiply by 2^o.
 """
 from __future__ import annotations
 
@@ -114,3 +117,24 @@ def weight_f32(seed: int, idx, sigma: float) -> np.ndarray:
 def uniform_u32(seed: int, stream: int, sub: int, idx) -> np.ndarray:
     """First Philox output word at indices `idx` (uniform on [0, 2^32))."""
     return _words(seed, stream, sub, idx)[0]
+
+
+def grad_fp16(seed: int, sub: int, idx, log2_scale: int, outlier_frac: float = 0.0,
+              outlier_log2: int = 0) -> np.ndarray:
+    """fp16 gradient values as raw binary16 bit patterns (uint16): the
+    Irwin-Hall integer z of the normal mapping, floor(z / 512) in
+    [-1024, 1023], times 2^log2_scale (times 2^outlier_log2 for outliers;
+    large outliers overflow to inf on purpose)."""
+    w = _words(seed, STREAM_GRAD, sub, idx)
+    s = np.zeros(np.shape(idx), dtype=np.int64)
+    for x in w:
+        x = x.astype(np.int64)
+        s += (x & 0xFFFF) + (x >> 16)
+    k = (2 * s - 8 * 65535) // 512
+    e = np.full(np.shape(idx), log2_scale, dtype=np.int64)
+    if outlier_frac > 0.0:
+        u = _words(seed, STREAM_OUTLIER, sub, idx)[0]
+        e = np.where(u < np.uint32(outlier_threshold(outlier_frac)), e + outlier_log2, e)
+    v = np.ldexp(k.astype(np.float32), e.astype(np.int32)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        return v.astype(np.float16).view(np.uint16)

@@ -93,6 +93,30 @@ def _floor_ps_build(*a, **k):
 
 
 _orig_build = oplan.build_partition
+_orig_unscale = ostep.unscale_and_clip
+
+
+def _unscale_forgets_scale(plan, st, max_norm, scale):
+    norm, coef, skip = _orig_unscale(plan, st, max_norm, scale)
+    return norm, (coef * np.float32(scale) if not skip else coef), skip
+
+
+class _GreedyScaler(ostep.LossScaler):
+    def update(self, overflow):
+        if overflow:
+            self.scale = max(self.scale / self.factor, self.min_scale)
+        else:
+            self.scale = self.scale * self.factor
+
+
+def _fp16_pin_unscale():
+    from tests import test_oracle_fp16 as f16
+    f16.test_fp16_step_matches_textbook_adamw_on_unscaled_gradients()
+
+
+def _fp16_pin_schedule():
+    from tests import test_oracle_fp16 as f16
+    f16.test_loss_scaler_schedule_by_hand()
 
 MUTANTS = [
     ("divide by N-1", ostep, "reduce_mean_bf16", _rm_divisor,
@@ -113,6 +137,10 @@ MUTANTS = [
      pins.test_gather_order_independent_and_views),
     ("partition size rounded down", oplan, "build_partition", _floor_ps_build,
      lambda: pins.test_partition_bruteforce(3)),
+    ("coefficient not unscaled", ostep, "unscale_and_clip", _unscale_forgets_scale,
+     _fp16_pin_unscale),
+    ("loss scale grows every good step", ostep, "LossScaler", _GreedyScaler,
+     _fp16_pin_schedule),
 ]
 
 
