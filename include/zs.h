@@ -75,6 +75,14 @@ typedef int32_t zs_status;
  * as kernel arguments). */
 #define ZS_MAX_RANKS 256
 
+/* 16-bit storage of gradients and parameters (zs_config.dtype): IEEE
+ * bfloat16, or IEEE binary16 for fp16 mixed precision with a loss scale
+ * ([Core flow] §1 table stores parameters and gradients in fp16).  All
+ * arithmetic is float32 either way; the dtype changes only the conversions
+ * (round to nearest even; an fp16 overflow becomes inf). */
+#define ZS_DTYPE_BF16 0
+#define ZS_DTYPE_FP16 1
+
 /* Bits of the device flag word written by zs_grad_norm / zs_shard_step. */
 #define ZS_SKIP_NONFINITE 1   /* gradient norm not finite: update skipped */
 
@@ -87,7 +95,7 @@ typedef struct zs_plan zs_plan;   /* opaque, host memory */
  * counted in per-rank shard elements). */
 typedef struct {
     int32_t n_ranks;                      /* N >= 1                              */
-    int32_t reserved;                     /* must be 0                           */
+    int32_t dtype;                        /* ZS_DTYPE_BF16 (default) or FP16     */
     int64_t param_persistence_threshold;  /* persistent iff numel < threshold    */
     int64_t reduce_bucket_size;           /* elements, >= 1                      */
     int64_t prefetch_bucket_size;         /* elements, >= 1 (gather buckets)     */
@@ -103,7 +111,7 @@ typedef struct {
 typedef struct {
     int32_t n_ranks, n_params;
     int32_t n_reduce_buckets, n_gather_buckets;
-    int32_t n_sub_groups, reserved;
+    int32_t n_sub_groups, dtype;
     int64_t psi;                    /* sum of numel                                   */
     int64_t shard_elems;            /* S: length of one shard row (multiple of 8)     */
     int64_t shard_elems_logical;    /* sum of ps over partitioned parameters          */
@@ -268,6 +276,41 @@ zs_status zs_grad_norm(const zs_plan *plan, const void *grad_shards, const void 
                        double *norm_scratch, int32_t recompute, float max_norm, float *d_norm,
                        float *d_clip_coef, int32_t *d_flags, void *stream);
 
+/* Dynamic loss scale for fp16 gradients, kept in device memory so that no
+ * host synchronisation is needed.  d_scale holds the scale S the caller
+ * multiplied the loss by for this step; d_good_steps the number of steps
+ * since the last overflow.  After the norm: on an overflow (non-finite
+ * norm) S = max(S / scale_factor, min_scale) and the count restarts; after
+ * scale_window consecutive good steps S = S * scale_factor (float32).  The
+ * pages name the unscale step only ([ZeRO-3 chapter] §6.3,
+ * unscale_and_clip_grads); this schedule is DeepSpeed's dynamic loss
+ * scaler without hysteresis.  d_good_steps may be NULL when
+ * scale_window <= 0: the scale is then static (read, never changed). */
+typedef struct {
+    float   *d_scale;        /* device, in/out                               */
+    int32_t *d_good_steps;   /* device, in/out (NULL: static scale)          */
+    float    scale_factor;   /* > 1, e.g. 2                                  */
+    float    min_scale;      /* > 0, e.g. 1                                  */
+    int32_t  scale_window;   /* e.g. 1000; <= 0: static scale                */
+    int32_t  reserved;       /* must be 0                                    */
+} zs_loss_scaler;
+
+/* A3 with a loss scale — unscale_and_clip_grads ([ZeRO-3 chapter] §6.3):
+ * the stored (reduced) gradients are the gradients of the loss times S.
+ * norm = float32(sqrt(sum of squares)) / S, the norm of the true gradients,
+ * written to d_norm; clip = min(1, max_norm / (norm + 1e-6)) (1 when
+ * max_norm <= 0); d_clip_coef = clip / S, the factor zs_adam_step and
+ * zs_adam_gather apply to the stored gradients; a non-finite norm (an
+ * overflow) sets ZS_SKIP_NONFINITE and reports coef 1.  Then the scaler is
+ * updated as described at zs_loss_scaler.  With S = 1 and a static scale
+ * this is zs_grad_norm exactly.  Other arguments as zs_grad_norm.  Errors:
+ * ZS_EINVAL (NULL scaler or d_scale, bad factor / min_scale, reserved != 0),
+ * ZS_ESTATE, ZS_ECUDA. */
+zs_status zs_unscale_and_clip(const zs_plan *plan, const void *grad_shards,
+                              const void *persist_grads, double *norm_scratch, int32_t recompute,
+                              float max_norm, const zs_loss_scaler *scaler, float *d_norm,
+                              float *d_clip_coef, int32_t *d_flags, void *stream);
+
 /* Size, in doubles, of the norm scratch array built into the library for
  * zs_grad_norm_noalloc (8 MiB of device memory per GPU that loads it). */
 #define ZS_NOALLOC_NORM_MAX_SCRATCH (1LL << 20)
@@ -366,6 +409,15 @@ zs_status zs_shard_step(const zs_plan *plan, const void *const *d_rank_grads,
                         const zs_adam_hparams *hp, int64_t step, float max_norm,
                         float *d_norm, float *d_clip_coef, int32_t *d_flags,
                         void *flat_out, void *stream);
+
+/* A6 with a loss scale: zs_reduce_scatter_all -> zs_unscale_and_clip
+ * (recompute 0) -> zs_adam_gather, for fp16 plans (any plan works).  Same
+ * arguments as zs_shard_step plus the scaler.  Errors as zs_shard_step. */
+zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_grads,
+                               const zs_shard_state *st, double *norm_scratch,
+                               const zs_adam_hparams *hp, int64_t step, float max_norm,
+                               const zs_loss_scaler *scaler, float *d_norm, float *d_clip_coef,
+                               int32_t *d_flags, void *flat_out, void *stream);
 
 #ifdef __cplusplus
 }

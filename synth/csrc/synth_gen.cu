@@ -8,6 +8,7 @@
 //   c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0),  k += (W0, W1)
 // Counter layout: (index lo, index hi, sub, stream), key: (seed lo, seed hi).
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace {
@@ -62,6 +63,24 @@ __global__ void normal_kernel(float *out, int64_t start, int64_t count, uint32_t
         out[i] = normal(philox((uint64_t)(start + i), sub, stream, k0, k1), c);
 }
 
+// fp16: floor(z / 512) * 2^e, exactly representable in binary16
+__global__ void grad_fp16_kernel(uint16_t *out, int64_t start, int64_t count, uint32_t k0,
+                                 uint32_t k1, uint32_t sub, int e, uint32_t othr, int oe) {
+    for (int64_t i = (int64_t)blockIdx.x * THREADS + threadIdx.x; i < count;
+         i += (int64_t)gridDim.x * THREADS) {
+        const uint64_t idx = (uint64_t)(start + i);
+        const uint4 w = philox(idx, sub, STREAM_GRAD, k0, k1);
+        const int32_t s = (int32_t)((w.x & 0xFFFFu) + (w.x >> 16) + (w.y & 0xFFFFu) + (w.y >> 16) +
+                                    (w.z & 0xFFFFu) + (w.z >> 16) + (w.w & 0xFFFFu) + (w.w >> 16));
+        const int32_t z = 2 * s - 8 * 65535;
+        const int32_t k = (z >= 0) ? (z / 512) : -((-z + 511) / 512);  // floor(z / 512)
+        int ee = e;
+        if (othr != 0u && philox(idx, sub, STREAM_OUTLIER, k0, k1).x < othr) ee += oe;
+        const float v = ldexpf((float)k, ee);
+        out[i] = __half_as_ushort(__float2half_rn(v));
+    }
+}
+
 unsigned blocks_for(int64_t count) {
     int64_t b = (count + THREADS - 1) / THREADS;
     if (b > 152 * 16) b = 152 * 16;
@@ -79,6 +98,16 @@ int zsg_fill_grad_bf16(void *out, int64_t start, int64_t count, uint64_t seed, u
     grad_kernel<<<blocks_for(count), THREADS, 0, (cudaStream_t)stream>>>(
         static_cast<uint16_t *>(out), start, count, (uint32_t)seed, (uint32_t)(seed >> 32), sub, c,
         outlier_thr, outlier_scale);
+    return (int)cudaGetLastError();
+}
+
+// out[i] = fp16 gradient value (binary16 bits, exact) at index start + i.
+int zsg_fill_grad_fp16(void *out, int64_t start, int64_t count, uint64_t seed, uint32_t sub,
+                       int log2_scale, uint32_t outlier_thr, int outlier_log2, void *stream) {
+    if (count <= 0) return 0;
+    grad_fp16_kernel<<<blocks_for(count), THREADS, 0, (cudaStream_t)stream>>>(
+        static_cast<uint16_t *>(out), start, count, (uint32_t)seed, (uint32_t)(seed >> 32), sub,
+        log2_scale, outlier_thr, outlier_log2);
     return (int)cudaGetLastError();
 }
 

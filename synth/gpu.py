@@ -20,6 +20,9 @@ def _load():
         lib.zsg_fill_grad_bf16.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_uint64,
                                            C.c_uint32, C.c_float, C.c_uint32, C.c_float,
                                            C.c_void_p]
+        lib.zsg_fill_grad_fp16.restype = C.c_int
+        lib.zsg_fill_grad_fp16.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_uint64,
+                                           C.c_uint32, C.c_int, C.c_uint32, C.c_int, C.c_void_p]
         lib.zsg_fill_normal_f32.restype = C.c_int
         lib.zsg_fill_normal_f32.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_uint64,
                                             C.c_uint32, C.c_uint32, C.c_float, C.c_void_p]
@@ -51,3 +54,13 @@ def fill_weight_f32(t, start: int, seed: int, sigma: float, stream=None) -> None
                                       _stream(stream))
     if err:
         raise RuntimeError(f"zsg_fill_normal_f32: CUDA error {err}")
+
+
+def fill_grad_fp16(t, start: int, seed: int, log2_scale: int, outlier_frac: float = 0.0,
+                   outlier_log2: int = 0, sub: int = 0, stream=None) -> None:
+    """t (2-byte CUDA tensor)[i] = philox.grad_fp16(seed, sub, start + i, ...)."""
+    thr = philox.outlier_threshold(outlier_frac) if outlier_frac > 0 else 0
+    err = _load().zsg_fill_grad_fp16(t.data_ptr(), int(start), t.numel(), int(seed), sub,
+                                     int(log2_scale), thr, int(outlier_log2), _stream(stream))
+    if err:
+        raise RuntimeError(f"zsg_fill_grad_fp16: CUDA error {err}")

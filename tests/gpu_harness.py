@@ -69,12 +69,16 @@ class Guarded:
 
 class DevicePlan:
     def __init__(self, numel, N, threshold=100_000, B=5_000_000, G=50_000_000, U=10**9,
-                 ds_id=None, seed=1234, sigma=1e-2, outlier=0.0, device="cuda:0"):
+                 ds_id=None, seed=1234, sigma=1e-2, outlier=0.0, device="cuda:0", dtype="bf16",
+                 log2_scale=-4, outlier_log2=0):
         self.dev = torch.device(device)
         self.numel, self.N, self.seed, self.sigma, self.outlier = numel, N, seed, sigma, outlier
+        self.dtype, self.log2_scale, self.outlier_log2 = dtype, log2_scale, outlier_log2
         self.op = oplan.build_partition(numel, N, threshold=threshold, reduce_bucket_size=B,
-                                        prefetch_bucket_size=G, sub_group_size=U, ds_id=ds_id)
+                                        prefetch_bucket_size=G, sub_group_size=U, ds_id=ds_id,
+                                        dtype=dtype)
         cfg = zs.zs_default_config(N)
+        cfg.dtype = zs.ZS_DTYPE_FP16 if dtype == "fp16" else zs.ZS_DTYPE_BF16
         cfg.param_persistence_threshold = threshold
         cfg.reduce_bucket_size = B
         cfg.prefetch_bucket_size = G
@@ -117,11 +121,21 @@ class DevicePlan:
         total = sum(N * L for L in op.bucket_buf_elems)
         if use_gpu_generator:
             pool = torch.empty(max(total, 8), dtype=torch.int16, device=self.dev)
-            sgpu.fill_grad_bf16(pool, 0, step_seed, self.sigma, self.outlier)
+            if self.dtype == "fp16":
+                sgpu.fill_grad_fp16(pool, 0, step_seed, self.log2_scale, self.outlier,
+                                    self.outlier_log2)
+            else:
+                sgpu.fill_grad_bf16(pool, 0, step_seed, self.sigma, self.outlier)
             host = pool.cpu().numpy().view(np.uint16)
         else:
-            host = philox.grad_bf16(step_seed, 0, np.arange(total, dtype=np.uint64), self.sigma,
-                                    self.outlier) if total else np.zeros(0, np.uint16)
+            idx = np.arange(total, dtype=np.uint64)
+            if not total:
+                host = np.zeros(0, np.uint16)
+            elif self.dtype == "fp16":
+                host = philox.grad_fp16(step_seed, 0, idx, self.log2_scale, self.outlier,
+                                        self.outlier_log2)
+            else:
+                host = philox.grad_bf16(step_seed, 0, idx, self.sigma, self.outlier)
             pool = torch.from_numpy(host.view(np.int16).copy()).to(self.dev)
         self.grad_bufs, self.ptrs, run = [], [], 0
         for L in op.bucket_buf_elems:
@@ -200,6 +214,19 @@ def bf16_ulp(x_u16):
     v = np.abs(bf16_to_f32(x_u16).astype(np.float64))
     e = np.floor(np.log2(np.maximum(v, 2.0 ** -133)))
     return np.maximum(2.0 ** (e - 7), 2.0 ** -133)
+
+
+def fp16_ulp(x_u16):
+    v = np.abs(np.asarray(x_u16, np.uint16).view(np.float16).astype(np.float64))
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -24)))
+    return np.maximum(2.0 ** (e - 10), 2.0 ** -24)
+
+
+def assert_fp16_within_ulp(a_u16, b_u16, what):
+    a = np.asarray(a_u16, np.uint16).view(np.float16).astype(np.float64)
+    b = np.asarray(b_u16, np.uint16).view(np.float16).astype(np.float64)
+    bad = np.abs(a - b) > fp16_ulp(b_u16) * (1 + 1e-9)
+    assert not bad.any(), f"{what}: {int(bad.sum())} values more than 1 fp16 ulp away"
 
 
 def assert_bf16_within_ulp(a_u16, b_u16, what):

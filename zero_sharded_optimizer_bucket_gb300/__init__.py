@@ -27,6 +27,7 @@ _lib = C.CDLL(LIB_PATH)
 ZS_OK, ZS_EINVAL, ZS_ENOMEM, ZS_ECUDA, ZS_ESTATE, ZS_ETIMEOUT = 0, -1, -2, -3, -4, -5
 ZS_MAX_RANKS = 256
 ZS_SKIP_NONFINITE = 1
+ZS_DTYPE_BF16, ZS_DTYPE_FP16 = 0, 1
 ZS_NOALLOC_NORM_MAX_SCRATCH = 1 << 20
 TILE_DTYPE = [("dst", "<i8"), ("src", "<i8"), ("flat", "<i8"), ("win", "<i8"),
               ("len", "<i4"), ("valid", "<i4"), ("flat_len", "<i4"), ("bucket", "<i4")]
@@ -39,7 +40,7 @@ class ZsError(RuntimeError):
 
 
 class zs_config(C.Structure):
-    _fields_ = [("n_ranks", C.c_int32), ("reserved", C.c_int32),
+    _fields_ = [("n_ranks", C.c_int32), ("dtype", C.c_int32),
                 ("param_persistence_threshold", C.c_int64), ("reduce_bucket_size", C.c_int64),
                 ("prefetch_bucket_size", C.c_int64), ("sub_group_size", C.c_int64)]
 
@@ -52,7 +53,7 @@ class zs_adam_hparams(C.Structure):
 
 class zs_plan_info_t(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("n_ranks", "n_params", "n_reduce_buckets",
-                                         "n_gather_buckets", "n_sub_groups", "reserved")] + \
+                                         "n_gather_buckets", "n_sub_groups", "dtype")] + \
                [(n, C.c_int64) for n in ("psi", "shard_elems", "shard_elems_logical",
                                          "persist_elems", "persist_elems_logical", "flat_elems",
                                          "padding_elems", "max_bucket_buf_elems",
@@ -81,6 +82,11 @@ class zs_gather_bucket_info_t(C.Structure):
 class zs_sub_group_info_t(C.Structure):
     _fields_ = [("n_params", C.c_int32), ("reserved", C.c_int32), ("shard_lo", C.c_int64),
                 ("shard_hi", C.c_int64), ("persist_lo", C.c_int64), ("persist_hi", C.c_int64)]
+
+
+class zs_loss_scaler(C.Structure):
+    _fields_ = [("d_scale", C.c_void_p), ("d_good_steps", C.c_void_p), ("scale_factor", C.c_float),
+                ("min_scale", C.c_float), ("scale_window", C.c_int32), ("reserved", C.c_int32)]
 
 
 class zs_shard_state(C.Structure):
@@ -127,6 +133,11 @@ _sig("zs_reduce_scatter_all", _i32, [_P, _P, _P, _P, _P, _P])
 _sig("zs_adam_gather", _i32, [_P, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                               C.POINTER(zs_shard_state), _P, _P])
 _sig("zs_grad_norm_noalloc", _i32, [_P, _P, _P, _f32, _P, _P, _P, _P])
+_sig("zs_unscale_and_clip", _i32, [_P, _P, _P, _P, _i32, _f32, C.POINTER(zs_loss_scaler), _P,
+                                   _P, _P, _P])
+_sig("zs_shard_step_scaled", _i32, [_P, _P, C.POINTER(zs_shard_state), _P,
+                                    C.POINTER(zs_adam_hparams), _i64, _f32,
+                                    C.POINTER(zs_loss_scaler), _P, _P, _P, _P, _P])
 _sig("zs_shard_step", _i32, [_P, _P, C.POINTER(zs_shard_state), _P, C.POINTER(zs_adam_hparams),
                              _i64, _f32, _P, _P, _P, _P, _P])
 
@@ -376,3 +387,30 @@ def zs_grad_norm_noalloc(plan, grad_shards, persist_grads, max_norm: float, d_no
     _check(_lib.zs_grad_norm_noalloc(_h(plan), _ptr(grad_shards), _ptr(persist_grads),
                                      float(max_norm), _ptr(d_norm), _ptr(d_clip_coef),
                                      _ptr(d_flags), _stream(stream)), "zs_grad_norm_noalloc")
+
+
+def make_loss_scaler(d_scale, d_good_steps=None, scale_factor=2.0, min_scale=1.0,
+                     scale_window=1000) -> zs_loss_scaler:
+    """zs_loss_scaler from device tensors / addresses (float32 scale, int32 count)."""
+    return zs_loss_scaler(_ptr(d_scale), _ptr(d_good_steps), float(scale_factor),
+                          float(min_scale), int(scale_window), 0)
+
+
+def zs_unscale_and_clip(plan, grad_shards, persist_grads, norm_scratch, recompute: bool,
+                        max_norm: float, scaler: zs_loss_scaler, d_norm, d_clip_coef, d_flags,
+                        stream=None) -> None:
+    _check(_lib.zs_unscale_and_clip(_h(plan), _ptr(grad_shards), _ptr(persist_grads),
+                                    _ptr(norm_scratch), 1 if recompute else 0, float(max_norm),
+                                    C.byref(scaler), _ptr(d_norm), _ptr(d_clip_coef),
+                                    _ptr(d_flags), _stream(stream)), "zs_unscale_and_clip")
+
+
+def zs_shard_step_scaled(plan, d_rank_grads, state: zs_shard_state, norm_scratch, hp, step: int,
+                         max_norm: float, scaler: zs_loss_scaler, d_norm, d_clip_coef, d_flags,
+                         flat_out, stream=None) -> None:
+    h = _hp(hp)
+    _check(_lib.zs_shard_step_scaled(_h(plan), _ptr(d_rank_grads), C.byref(state),
+                                     _ptr(norm_scratch), C.byref(h), int(step), float(max_norm),
+                                     C.byref(scaler), _ptr(d_norm), _ptr(d_clip_coef),
+                                     _ptr(d_flags), _ptr(flat_out), _stream(stream)),
+           "zs_shard_step_scaled")

@@ -116,7 +116,7 @@ zs_status zs_partition(const zs_plan *P, const float *W, const zs_shard_state *s
     if (r) return r;
     if ((r = check_state(P, st, false, true, fn))) return r;
     if (P->psi > 0 && !al(W, 4)) return zs_fail(ZS_EINVAL, "%s: full_params NULL or misaligned", fn);
-    return cuda_status(zsl_partition(P->d_tiles, (int64_t)P->tiles.size(), W, *st,
+    return cuda_status(zsl_partition(P->d_tiles, (int64_t)P->tiles.size(), P->cfg.dtype, W, *st,
                                      (cudaStream_t)stream), fn);
 }
 
@@ -143,6 +143,7 @@ zs_status zs_reduce_scatter(const zs_plan *P, int32_t bucket, const void *const 
         return zs_fail(ZS_EINVAL, "%s: norm_scratch not 8-byte aligned", fn);
     const ZsBucket &b = P->buckets[bucket];
     return cuda_status(zsl_reduce_scatter(P->d_tiles, b.first_tile, b.n_tiles, rank_grads, N,
+                                          P->cfg.dtype,
                                           static_cast<uint16_t *>(grad_shards),
                                           static_cast<uint16_t *>(persist_grads), norm_scratch,
                                           (cudaStream_t)stream), fn);
@@ -162,10 +163,10 @@ zs_status zs_grad_norm(const zs_plan *P, const void *grad_shards, const void *pe
         if (P->Pn_alloc > 0 && !al(persist_grads, 16))
             return zs_fail(ZS_EINVAL, "%s: persist_grads NULL or not 16-byte aligned", fn);
     }
-    return cuda_status(zsl_norm(P->d_tiles, (int64_t)P->tiles.size(), P->n_level1,
+    return cuda_status(zsl_norm(P->d_tiles, (int64_t)P->tiles.size(), P->n_level1, P->cfg.dtype,
                                 static_cast<const uint16_t *>(grad_shards),
                                 static_cast<const uint16_t *>(persist_grads), norm_scratch,
-                                recompute != 0, max_norm, d_norm, d_clip_coef, d_flags,
+                                recompute != 0, max_norm, d_norm, d_clip_coef, d_flags, nullptr,
                                 (cudaStream_t)stream), fn);
 }
 
@@ -187,7 +188,7 @@ zs_status zs_adam_step(const zs_plan *P, int32_t sub_group, const zs_adam_hparam
         const ZsSubGroup &g = P->sub_groups[sub_group];
         s_lo = g.s_lo; s_hi = g.s_hi; p_lo = g.p_lo; p_hi = g.p_hi;
     }
-    return cuda_status(zsl_adam(P->cfg.n_ranks, P->S, s_lo, s_hi, p_lo, p_hi, c, d_clip_coef,
+    return cuda_status(zsl_adam(P->cfg.n_ranks, P->cfg.dtype, P->S, s_lo, s_hi, p_lo, p_hi, c, d_clip_coef,
                                 d_flags, *st, (cudaStream_t)stream), fn);
 }
 
@@ -259,6 +260,43 @@ zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *pa
     return ZS_OK;
 }
 
+zs_status zs_unscale_and_clip(const zs_plan *P, const void *grad_shards, const void *persist_grads,
+                              double *norm_scratch, int32_t recompute, float max_norm,
+                              const zs_loss_scaler *scaler, float *d_norm, float *d_clip_coef,
+                              int32_t *d_flags, void *stream) {
+    const char *fn = "zs_unscale_and_clip";
+    zs_status r = need_table(P, fn);
+    if (r) return r;
+    if (!scaler || !al(scaler->d_scale, 4))
+        return zs_fail(ZS_EINVAL, "%s: scaler or its d_scale NULL / misaligned", fn);
+    if (scaler->reserved != 0) return zs_fail(ZS_EINVAL, "%s: scaler reserved field must be 0", fn);
+    if (scaler->scale_window > 0) {
+        if (!al(scaler->d_good_steps, 4))
+            return zs_fail(ZS_EINVAL, "%s: d_good_steps NULL or misaligned", fn);
+        if (!(scaler->scale_factor > 1.0f) || !(scaler->min_scale > 0.0f))
+            return zs_fail(ZS_EINVAL, "%s: need scale_factor > 1 and min_scale > 0", fn);
+    }
+    if ((r = check_scratch(P, norm_scratch, fn))) return r;
+    if ((r = check_scalars(d_norm, d_clip_coef, d_flags, fn))) return r;
+    if (recompute) {
+        if (P->S > 0 && !al(grad_shards, 16))
+            return zs_fail(ZS_EINVAL, "%s: grad_shards NULL or not 16-byte aligned", fn);
+        if (P->Pn_alloc > 0 && !al(persist_grads, 16))
+            return zs_fail(ZS_EINVAL, "%s: persist_grads NULL or not 16-byte aligned", fn);
+    }
+    ZsScaleArgs sc;
+    sc.d_scale = scaler->d_scale;
+    sc.d_good = scaler->scale_window > 0 ? scaler->d_good_steps : nullptr;
+    sc.factor = scaler->scale_factor;
+    sc.min_scale = scaler->min_scale;
+    sc.window = scaler->scale_window;
+    return cuda_status(zsl_norm(P->d_tiles, (int64_t)P->tiles.size(), P->n_level1, P->cfg.dtype,
+                                static_cast<const uint16_t *>(grad_shards),
+                                static_cast<const uint16_t *>(persist_grads), norm_scratch,
+                                recompute != 0, max_norm, d_norm, d_clip_coef, d_flags, &sc,
+                                (cudaStream_t)stream), fn);
+}
+
 zs_status zs_reduce_scatter_all(const zs_plan *P, const void *const *d_rank_grads,
                                 void *grad_shards, void *persist_grads, double *norm_scratch,
                                 void *stream) {
@@ -275,7 +313,8 @@ zs_status zs_reduce_scatter_all(const zs_plan *P, const void *const *d_rank_grad
         return zs_fail(ZS_EINVAL, "%s: persist_grads NULL or not 16-byte aligned", fn);
     if ((r = check_scratch(P, norm_scratch, fn))) return r;
     return cuda_status(zsl_reduce_scatter_all(P->d_tiles, (int64_t)P->tiles.size(), d_rank_grads,
-                                              P->cfg.n_ranks, static_cast<uint16_t *>(grad_shards),
+                                              P->cfg.n_ranks, P->cfg.dtype,
+                                              static_cast<uint16_t *>(grad_shards),
                                               static_cast<uint16_t *>(persist_grads), norm_scratch,
                                               (cudaStream_t)stream), fn);
 }
@@ -293,7 +332,7 @@ zs_status zs_adam_gather(const zs_plan *P, const zs_adam_hparams *hp, int64_t st
         return zs_fail(ZS_EINVAL, "%s: d_clip_coef / d_flags NULL or misaligned", fn);
     if (P->flat_elems > 0 && !al(flat_out, 2))
         return zs_fail(ZS_EINVAL, "%s: flat_out NULL or odd address", fn);
-    return cuda_status(zsl_step2(P->d_tiles, (int64_t)P->tiles.size(), c, d_clip_coef, d_flags,
+    return cuda_status(zsl_step2(P->d_tiles, (int64_t)P->tiles.size(), P->cfg.dtype, c, d_clip_coef, d_flags,
                                  *st, static_cast<uint16_t *>(flat_out), (cudaStream_t)stream), fn);
 }
 
@@ -316,6 +355,33 @@ zs_status zs_shard_step(const zs_plan *P, const void *const *d_rank_grads,
         return r;
     if ((r = zs_grad_norm(P, st->grad_shards, st->persist_grads, norm_scratch, 0, max_norm, d_norm,
                           d_clip_coef, d_flags, stream)))
+        return r;
+    return zs_adam_gather(P, hp, step, d_clip_coef, d_flags, st, flat_out, stream);
+}
+
+zs_status zs_shard_step_scaled(const zs_plan *P, const void *const *d_rank_grads,
+                               const zs_shard_state *st, double *norm_scratch,
+                               const zs_adam_hparams *hp, int64_t step, float max_norm,
+                               const zs_loss_scaler *scaler, float *d_norm, float *d_clip_coef,
+                               int32_t *d_flags, void *flat_out, void *stream) {
+    const char *fn = "zs_shard_step_scaled";
+    zs_status r = need_table(P, fn);
+    if (r) return r;
+    ZsAdamScalars c;
+    if ((r = adam_scalars(hp, step, &c, fn))) return r;
+    if ((r = check_state(P, st, true, true, fn))) return r;
+    if ((r = check_scratch(P, norm_scratch, fn))) return r;
+    if ((r = check_scalars(d_norm, d_clip_coef, d_flags, fn))) return r;
+    if (!scaler || !al(scaler->d_scale, 4) || scaler->reserved != 0 ||
+        (scaler->scale_window > 0 && !al(scaler->d_good_steps, 4)))
+        return zs_fail(ZS_EINVAL, "%s: bad loss scaler", fn);
+    if (P->flat_elems > 0 && !al(flat_out, 2))
+        return zs_fail(ZS_EINVAL, "%s: flat_out NULL or odd address", fn);
+    if ((r = zs_reduce_scatter_all(P, d_rank_grads, st->grad_shards, st->persist_grads,
+                                   norm_scratch, stream)))
+        return r;
+    if ((r = zs_unscale_and_clip(P, st->grad_shards, st->persist_grads, norm_scratch, 0, max_norm,
+                                 scaler, d_norm, d_clip_coef, d_flags, stream)))
         return r;
     return zs_adam_gather(P, hp, step, d_clip_coef, d_flags, st, flat_out, stream);
 }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -60,20 +61,42 @@ __device__ __forceinline__ uint4 mask8(const uint4 &v, int64_t lo, int64_t hi) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Sum of squares of 8 bf16 values for the norm partial.  In float32 when
-// that can neither overflow nor lose the whole group to underflow (largest
-// |x| in [2^-64, 2^60)), in float64 otherwise (and for Inf / NaN, which
-// then propagate).  Fixed order, no contraction: the value depends only on
-// the 8 inputs, so every kernel that calls it gets the same bits.
+// 16-bit storage types: bit pattern <-> float.
+struct BF16T {
+    static __device__ __forceinline__ float to_f32(uint32_t b) { return bf2f(b); }
+    static __device__ __forceinline__ uint32_t from_f32(float x) { return f2bf(x); }
+    // largest |x| (bits & 0x7FFF) for which the squares of 8 values neither
+    // overflow float32 (|x| < 2^60) nor all underflow (|x| >= 2^-64)
+    static __device__ __forceinline__ bool sq_in_f32(uint32_t mx) {
+        return mx < 0x5D80u && (mx == 0u || mx >= 0x1F80u);
+    }
+};
+struct FP16T {
+    static __device__ __forceinline__ float to_f32(uint32_t b) {
+        return __half2float(__ushort_as_half((unsigned short)b));
+    }
+    static __device__ __forceinline__ uint32_t from_f32(float x) {
+        return (uint32_t)__half_as_ushort(__float2half_rn(x));
+    }
+    // binary16 squares (<= 65504^2, >= 2^-48) always fit float32
+    static __device__ __forceinline__ bool sq_in_f32(uint32_t) { return true; }
+};
+
+// Sum of squares of 8 16-bit values for the norm partial.  In float32 when
+// that can neither overflow nor lose the whole group to underflow, in
+// float64 otherwise (Inf / NaN propagate either way).  Fixed order, no
+// contraction: the value depends only on the 8 inputs, so every kernel that
+// calls it gets the same bits.
+template <class T>
 __device__ __forceinline__ void group_sq(const uint32_t r[8], float &acc32, double &acc64) {
     uint32_t mx = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) mx = max(mx, r[i] & 0x7FFFu);
-    if (mx >= 0x5D80u || (mx != 0u && mx < 0x1F80u)) {
+    if (!T::sq_in_f32(mx)) {
         double s = 0.0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const double v = (double)bf2f(r[i]);
+            const double v = (double)T::to_f32(r[i]);
             s = __dadd_rn(s, __dmul_rn(v, v));
         }
         acc64 = __dadd_rn(acc64, s);
@@ -81,7 +104,7 @@ __device__ __forceinline__ void group_sq(const uint32_t r[8], float &acc32, doub
         float s = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float v = bf2f(r[i]);
+            const float v = T::to_f32(r[i]);
             s = __fadd_rn(s, __fmul_rn(v, v));
         }
         acc32 = __fadd_rn(acc32, s);

@@ -12,27 +12,36 @@ struct ZsAdamScalars {
     int adamw;
 };
 
+// Loss scale of the norm finish (see zs_loss_scaler); d_scale NULL: S = 1.
+struct ZsScaleArgs {
+    float *d_scale;
+    int32_t *d_good;
+    float factor, min_scale;
+    int32_t window;
+};
+
 cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                               const void *const *rank_ptrs, int N, uint16_t *gs, uint16_t *gP,
-                               double *partials, cudaStream_t s);
+                               const void *const *rank_ptrs, int N, int dtype, uint16_t *gs,
+                               uint16_t *gP, double *partials, cudaStream_t s);
 
 cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
-                                   const void *const *d_table, int N, uint16_t *gs, uint16_t *gP,
-                                   double *partials, cudaStream_t s);
+                                   const void *const *d_table, int N, int dtype, uint16_t *gs,
+                                   uint16_t *gP, double *partials, cudaStream_t s);
 
-cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, const uint16_t *gs,
-                     const uint16_t *gP, double *scratch, bool recompute, float max_norm,
-                     float *d_norm, float *d_coef, int32_t *d_flags, cudaStream_t s);
+cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,
+                     const uint16_t *gs, const uint16_t *gP, double *scratch, bool recompute,
+                     float max_norm, float *d_norm, float *d_coef, int32_t *d_flags,
+                     const ZsScaleArgs *scale, cudaStream_t s);
 
-cudaError_t zsl_adam(int N, int64_t S, int64_t s_lo, int64_t s_hi, int64_t p_lo, int64_t p_hi,
+cudaError_t zsl_adam(int N, int dtype, int64_t S, int64_t s_lo, int64_t s_hi, int64_t p_lo, int64_t p_hi,
                      const ZsAdamScalars &c, const float *d_coef, const int32_t *d_flags,
                      const zs_shard_state &st, cudaStream_t s);
 
-cudaError_t zsl_step2(const ZsTile *d_tiles, int64_t ntiles, const ZsAdamScalars &c,
+cudaError_t zsl_step2(const ZsTile *d_tiles, int64_t ntiles, int dtype, const ZsAdamScalars &c,
                       const float *d_coef, const int32_t *d_flags, const zs_shard_state &st,
                       uint16_t *flat_out, cudaStream_t s);
 
-cudaError_t zsl_partition(const ZsTile *d_tiles, int64_t ntiles, const float *W,
+cudaError_t zsl_partition(const ZsTile *d_tiles, int64_t ntiles, int dtype, const float *W,
                           const zs_shard_state &st, cudaStream_t s);
 
 // One gather launch covers the output range [out_lo, out_hi) of flat_out,

@@ -82,10 +82,11 @@ extern "C" zs_status zs_grad_norm_noalloc(const zs_plan *P, const void *grad_sha
     // every scratch element read below is written first by the same call
     // (one partial per tile, one first-level sum per block), so what an
     // earlier call left in the array does not matter
-    const cudaError_t e = zsl_norm(P->d_tiles, ntiles, P->n_level1,
+    const cudaError_t e = zsl_norm(P->d_tiles, ntiles, P->n_level1, P->cfg.dtype,
                                    static_cast<const uint16_t *>(grad_shards),
                                    static_cast<const uint16_t *>(persist_grads), scratch, true,
-                                   max_norm, d_norm, d_clip_coef, d_flags, (cudaStream_t)stream);
+                                   max_norm, d_norm, d_clip_coef, d_flags, nullptr,
+                                   (cudaStream_t)stream);
     if (e != cudaSuccess)
         return zs_fail(ZS_ECUDA, "%s: %s (%s)", fn, cudaGetErrorName(e), cudaGetErrorString(e));
     zs_clear_error();

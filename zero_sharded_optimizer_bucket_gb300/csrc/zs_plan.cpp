@@ -253,7 +253,7 @@ const char *zs_version(void) { return "libzs 0.1 (sm_103a)"; }
 void zs_default_config(zs_config *cfg, int32_t n_ranks) {
     if (!cfg) return;
     cfg->n_ranks = n_ranks;
-    cfg->reserved = 0;
+    cfg->dtype = ZS_DTYPE_BF16;
     cfg->param_persistence_threshold = 100000;
     cfg->reduce_bucket_size = 5000000;
     cfg->prefetch_bucket_size = 50000000;
@@ -265,7 +265,8 @@ zs_status zs_build_partition(const zs_config *cfg, int32_t n_params, const int64
     if (!cfg || !out) return zs_fail(ZS_EINVAL, "zs_build_partition: NULL config or output");
     *out = nullptr;
     if (cfg->n_ranks < 1) return zs_fail(ZS_EINVAL, "zs_build_partition: n_ranks must be >= 1");
-    if (cfg->reserved != 0) return zs_fail(ZS_EINVAL, "zs_build_partition: reserved field must be 0");
+    if (cfg->dtype != ZS_DTYPE_BF16 && cfg->dtype != ZS_DTYPE_FP16)
+        return zs_fail(ZS_EINVAL, "zs_build_partition: dtype must be ZS_DTYPE_BF16 or ZS_DTYPE_FP16");
     if (cfg->reduce_bucket_size < 1 || cfg->prefetch_bucket_size < 1 || cfg->sub_group_size < 1)
         return zs_fail(ZS_EINVAL, "zs_build_partition: bucket and sub-group sizes must be >= 1");
     if (n_params < 0 || (n_params > 0 && !numel))
@@ -300,6 +301,7 @@ zs_status zs_plan_info(const zs_plan *P, zs_plan_info_t *o) {
     o->n_reduce_buckets = (int32_t)P->buckets.size();
     o->n_gather_buckets = (int32_t)P->gathers.size();
     o->n_sub_groups = (int32_t)P->sub_groups.size();
+    o->dtype = P->cfg.dtype;
     o->psi = P->psi;
     o->shard_elems = P->S;
     o->shard_elems_logical = P->S_logical;

@@ -19,7 +19,7 @@ struct RankPtrs {
     const uint16_t *p[ZS_MAX_RANKS];
 };
 
-template <bool FROM_TABLE>
+template <bool FROM_TABLE, class T>
 __global__ void __launch_bounds__(THREADS, 5)
 rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
           const uint16_t *const *__restrict__ table, int N, float fN,
@@ -80,22 +80,22 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
                 for (int k = 0; k < N; ++k) {
                     const uint4 v = ldg16(p[k] + 8 * c);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], bf2f(lane16(v, i)));
+                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
                 }
             } else {
 #pragma unroll 4
                 for (int k = 0; k < N; ++k) {
                     const uint4 v = mask8(ldg16(p[k] + 8 * c), lo, hi);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], bf2f(lane16(v, i)));
+                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
                 }
             }
         }
         uint32_t r[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            r[i] = act ? f2bf(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN)) : 0u;
-        if (act) group_sq(r, sq32, sq64);
+            r[i] = act ? T::from_f32(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN)) : 0u;
+        if (act) group_sq<T>(r, sq32, sq64);
         const int64_t y0 = 8 * c - delta;  // destination of lane 0 of the chunk
         if (a == 0) {
             if (act) {
@@ -150,6 +150,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
 // Recompute the per-tile partial sums from the reduced gradients, with
 // the chunks and the thread mapping of rs_kernel (8-element chunks aligned in
 // the source, chunk gi on thread gi mod THREADS), so the same bits.
+template <class T>
 __global__ void __launch_bounds__(THREADS)
 norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__ gs,
                   const uint16_t *__restrict__ gP, double *__restrict__ partials) {
@@ -178,7 +179,7 @@ norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__
 #pragma unroll
             for (int i = 0; i < 8; ++i) r[i] = (i >= lo && i < hi) ? (uint32_t)in[y0 + i] : 0u;
         }
-        group_sq(r, sq32, sq64);
+        group_sq<T>(r, sq32, sq64);
     }
     const double s = block_sum(__dadd_rn((double)sq32, sq64), red);
     if (threadIdx.x == 0) partials[t] = s;
@@ -196,26 +197,48 @@ norm_level1_kernel(const double *__restrict__ partials, int64_t n, double *__res
     if (threadIdx.x == 0) level1[blockIdx.x] = s;
 }
 
-// Finish: total, norm = float(sqrt(total)), clip coefficient, flags.
+// Finish: total, norm = float(sqrt(total)) / S, clip coefficient / S,
+// flags; then the loss-scale update when a scaler is given.  S = 1 without
+// one, which leaves every result bit-identical to the unscaled formula.
 __global__ void __launch_bounds__(THREADS)
 norm_finish_kernel(const double *__restrict__ level1, int64_t n1, float max_norm,
                    float *__restrict__ d_norm, float *__restrict__ d_coef,
-                   int32_t *__restrict__ d_flags) {
+                   int32_t *__restrict__ d_flags, ZsScaleArgs sc) {
     __shared__ double red[WARPS];
     double v = 0.0;
     for (int64_t i = threadIdx.x; i < n1; i += THREADS) v = __dadd_rn(v, level1[i]);
     const double s = block_sum(v, red);
     if (threadIdx.x == 0) {
-        const float norm = (float)sqrt(s);
+        const float S = sc.d_scale ? *sc.d_scale : 1.0f;
+        const float norm = __fdiv_rn((float)sqrt(s), S);
         const bool finite = isfinite(norm);
         float coef = 1.0f;
-        if (finite && max_norm > 0.0f) {
-            const float c = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
-            coef = c < 1.0f ? c : 1.0f;
+        if (finite) {
+            float clip = 1.0f;
+            if (max_norm > 0.0f) {
+                const float c = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
+                clip = c < 1.0f ? c : 1.0f;
+            }
+            coef = __fdiv_rn(clip, S);
         }
         *d_norm = norm;
         *d_coef = coef;
         *d_flags = finite ? 0 : ZS_SKIP_NONFINITE;
+        if (sc.d_scale && sc.window > 0) {
+            if (!finite) {
+                const float d = __fdiv_rn(S, sc.factor);
+                *sc.d_scale = d > sc.min_scale ? d : sc.min_scale;
+                *sc.d_good = 0;
+            } else {
+                const int32_t g = *sc.d_good + 1;
+                if (g >= sc.window) {
+                    *sc.d_scale = __fmul_rn(S, sc.factor);
+                    *sc.d_good = 0;
+                } else {
+                    *sc.d_good = g;
+                }
+            }
+        }
     }
 }
 
@@ -223,35 +246,55 @@ norm_finish_kernel(const double *__restrict__ level1, int64_t n1, float max_norm
 
 using namespace zsk;
 
+template <class T>
+static cudaError_t launch_rs(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+                             const RankPtrs &p, const void *const *d_table, int N, uint16_t *gs,
+                             uint16_t *gP, double *partials, cudaStream_t s) {
+    if (d_table)
+        rs_kernel<true, T><<<(unsigned)ntiles, THREADS, 0, s>>>(
+            d_tiles, tile0, p, reinterpret_cast<const uint16_t *const *>(d_table), N, (float)N, gs,
+            gP, partials);
+    else
+        rs_kernel<false, T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, tile0, p, nullptr, N,
+                                                                 (float)N, gs, gP, partials);
+    return cudaGetLastError();
+}
+
 cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                               const void *const *rank_ptrs, int N, uint16_t *gs, uint16_t *gP,
-                               double *partials, cudaStream_t s) {
+                               const void *const *rank_ptrs, int N, int dtype, uint16_t *gs,
+                               uint16_t *gP, double *partials, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p;
     for (int k = 0; k < N; ++k) p.p[k] = static_cast<const uint16_t *>(rank_ptrs[k]);
-    rs_kernel<false><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, tile0, p, nullptr, N, (float)N,
-                                                          gs, gP, partials);
-    return cudaGetLastError();
+    return dtype == ZS_DTYPE_FP16
+               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, nullptr, N, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, nullptr, N, gs, gP, partials, s);
 }
 
 cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
-                                   const void *const *d_table, int N, uint16_t *gs, uint16_t *gP,
-                                   double *partials, cudaStream_t s) {
+                                   const void *const *d_table, int N, int dtype, uint16_t *gs,
+                                   uint16_t *gP, double *partials, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p = {};
-    rs_kernel<true><<<(unsigned)ntiles, THREADS, 0, s>>>(
-        d_tiles, 0, p, reinterpret_cast<const uint16_t *const *>(d_table), N, (float)N, gs, gP,
-        partials);
-    return cudaGetLastError();
+    return dtype == ZS_DTYPE_FP16
+               ? launch_rs<FP16T>(d_tiles, 0, ntiles, p, d_table, N, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, 0, ntiles, p, d_table, N, gs, gP, partials, s);
 }
 
-cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, const uint16_t *gs,
-                     const uint16_t *gP, double *scratch, bool recompute, float max_norm,
-                     float *d_norm, float *d_coef, int32_t *d_flags, cudaStream_t s) {
-    if (recompute && ntiles > 0)
-        norm_tiles_kernel<<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, gs, gP, scratch);
+cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,
+                     const uint16_t *gs, const uint16_t *gP, double *scratch, bool recompute,
+                     float max_norm, float *d_norm, float *d_coef, int32_t *d_flags,
+                     const ZsScaleArgs *scale, cudaStream_t s) {
+    if (recompute && ntiles > 0) {
+        if (dtype == ZS_DTYPE_FP16)
+            norm_tiles_kernel<FP16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, gs, gP, scratch);
+        else
+            norm_tiles_kernel<BF16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, gs, gP, scratch);
+    }
     norm_level1_kernel<<<(unsigned)n_level1, THREADS, 0, s>>>(scratch, ntiles, scratch + ntiles);
+    ZsScaleArgs sc = {};
+    if (scale) sc = *scale;
     norm_finish_kernel<<<1, THREADS, 0, s>>>(scratch + ntiles, n_level1, max_norm, d_norm, d_coef,
-                                             d_flags);
+                                             d_flags, sc);
     return cudaGetLastError();
 }

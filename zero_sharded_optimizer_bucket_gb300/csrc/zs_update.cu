@@ -47,6 +47,7 @@ __device__ __forceinline__ void store8f(float *a, const float o[8]) {
 }
 
 // 8 aligned elements at off: Adam on all of them, bf16 results in r.
+template <class T>
 __device__ __forceinline__ void adam8(const StatePtrs &s, int64_t off, float coef, const AdamC &c,
                                       uint32_t r[8]) {
     const uint4 gv = ldg16(s.g + off);
@@ -56,8 +57,8 @@ __device__ __forceinline__ void adam8(const StatePtrs &s, int64_t off, float coe
     load8f(s.v + off, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        adam_elem(p[i], m[i], v[i], bf2f(lane16(gv, i)), coef, c);
-        r[i] = f2bf(p[i]);
+        adam_elem(p[i], m[i], v[i], T::to_f32(lane16(gv, i)), coef, c);
+        r[i] = T::from_f32(p[i]);
     }
     store8f(s.p + off, p);
     store8f(s.m + off, m);
@@ -65,11 +66,12 @@ __device__ __forceinline__ void adam8(const StatePtrs &s, int64_t off, float coe
     *reinterpret_cast<uint4 *>(s.param + off) = pack8(r);
 }
 
+template <class T>
 __device__ __forceinline__ uint32_t adam1(const StatePtrs &s, int64_t x, float coef,
                                           const AdamC &c) {
     float p = s.p[x], m = s.m[x], v = s.v[x];
-    adam_elem(p, m, v, bf2f(s.g[x]), coef, c);
-    const uint32_t r = f2bf(p);
+    adam_elem(p, m, v, T::to_f32(s.g[x]), coef, c);
+    const uint32_t r = T::from_f32(p);
     s.p[x] = p;
     s.m[x] = m;
     s.v[x] = v;
@@ -79,6 +81,7 @@ __device__ __forceinline__ uint32_t adam1(const StatePtrs &s, int64_t x, float c
 
 // Unfused Adam over one sub-group: blockIdx.y < N walks shard row y,
 // columns [s_lo, s_lo + W); blockIdx.y == N walks persistent [p_lo, p_lo + PW).
+template <class T>
 __global__ void __launch_bounds__(THREADS)
 adam_kernel(int N, int64_t S, int64_t s_lo, int64_t W, int64_t p_lo, int64_t PW, AdamC c,
             const float *__restrict__ d_coef, const int32_t *__restrict__ d_flags,
@@ -92,13 +95,14 @@ adam_kernel(int N, int64_t S, int64_t s_lo, int64_t W, int64_t p_lo, int64_t PW,
     for (int64_t u = (int64_t)blockIdx.x * THREADS + threadIdx.x; u < units;
          u += (int64_t)gridDim.x * THREADS) {
         uint32_t r[8];
-        adam8(s, base + 8 * u, coef, c, r);
+        adam8<T>(s, base + 8 * u, coef, c, r);
     }
 }
 
 // Fused pass 2: Adam + cast on one tile, and the cast parameters also
 // written at their place in model flat space (the all-gather of the next
 // forward pass, [ZeRO-3 chapter] §5.2), straight from registers.
+template <class T>
 __global__ void __launch_bounds__(THREADS)
 step2_kernel(const ZsTile *__restrict__ tiles, AdamC c, const float *__restrict__ d_coef,
              const int32_t *__restrict__ d_flags, zs_shard_state st,
@@ -123,11 +127,11 @@ step2_kernel(const ZsTile *__restrict__ tiles, AdamC c, const float *__restrict_
         for (int i = 0; i < 8; ++i) r[i] = 0u;
         if (act) {
             if (x0 >= D && x0 + 8 <= D + L) {
-                adam8(s, x0, coef, c, r);
+                adam8<T>(s, x0, coef, c, r);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (x0 + i >= D && x0 + i < D + L) r[i] = adam1(s, x0 + i, coef, c);
+                    if (x0 + i >= D && x0 + i < D + L) r[i] = adam1<T>(s, x0 + i, coef, c);
             }
         }
         if (pers) continue;
@@ -171,6 +175,7 @@ step2_kernel(const ZsTile *__restrict__ tiles, AdamC c, const float *__restrict_
 }
 
 // Partition copy: dst <- W[win + i] (0 beyond valid), moments zero, bf16 shard.
+template <class T>
 __global__ void __launch_bounds__(THREADS)
 partition_kernel(const ZsTile *__restrict__ tiles, const float *__restrict__ W, zs_shard_state st) {
     const ZsTile tile = tiles[blockIdx.x];
@@ -186,7 +191,7 @@ partition_kernel(const ZsTile *__restrict__ tiles, const float *__restrict__ W, 
         for (int i = 0; i < 8; ++i) {
             const int64_t li = x0 + i - D;
             w[i] = (li >= 0 && li < tile.valid) ? __ldg(W + tile.win + li) : 0.0f;
-            r[i] = f2bf(w[i]);
+            r[i] = T::from_f32(w[i]);
         }
         if (x0 >= D && x0 + 8 <= D + L) {
             const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -220,9 +225,9 @@ __host__ AdamC to_device(const ZsAdamScalars &a) {
 
 using namespace zsk;
 
-cudaError_t zsl_adam(int N, int64_t S, int64_t s_lo, int64_t s_hi, int64_t p_lo, int64_t p_hi,
-                     const ZsAdamScalars &a, const float *d_coef, const int32_t *d_flags,
-                     const zs_shard_state &st, cudaStream_t s) {
+cudaError_t zsl_adam(int N, int dtype, int64_t S, int64_t s_lo, int64_t s_hi, int64_t p_lo,
+                     int64_t p_hi, const ZsAdamScalars &a, const float *d_coef,
+                     const int32_t *d_flags, const zs_shard_state &st, cudaStream_t s) {
     const int64_t W = s_hi - s_lo, PW = p_hi - p_lo;
     if ((W <= 0 || N == 0) && PW <= 0) return cudaSuccess;
     const int64_t units = (W > PW ? W : PW) / 8;
@@ -231,23 +236,35 @@ cudaError_t zsl_adam(int N, int64_t S, int64_t s_lo, int64_t s_hi, int64_t p_lo,
     if (x > cap) x = cap;
     if (x < 1) x = 1;
     dim3 grid((unsigned)x, (unsigned)(N + 1));
-    adam_kernel<<<grid, THREADS, 0, s>>>(N, S, s_lo, W, p_lo, PW, to_device(a), d_coef, d_flags, st);
+    if (dtype == ZS_DTYPE_FP16)
+        adam_kernel<FP16T><<<grid, THREADS, 0, s>>>(N, S, s_lo, W, p_lo, PW, to_device(a), d_coef,
+                                                    d_flags, st);
+    else
+        adam_kernel<BF16T><<<grid, THREADS, 0, s>>>(N, S, s_lo, W, p_lo, PW, to_device(a), d_coef,
+                                                    d_flags, st);
     return cudaGetLastError();
 }
 
-cudaError_t zsl_step2(const ZsTile *d_tiles, int64_t ntiles, const ZsAdamScalars &a,
+cudaError_t zsl_step2(const ZsTile *d_tiles, int64_t ntiles, int dtype, const ZsAdamScalars &a,
                       const float *d_coef, const int32_t *d_flags, const zs_shard_state &st,
                       uint16_t *flat_out, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     const int a0 = (int)((reinterpret_cast<uintptr_t>(flat_out) >> 1) & 7);
-    step2_kernel<<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, to_device(a), d_coef, d_flags, st,
-                                                      flat_out, a0);
+    if (dtype == ZS_DTYPE_FP16)
+        step2_kernel<FP16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, to_device(a), d_coef,
+                                                                 d_flags, st, flat_out, a0);
+    else
+        step2_kernel<BF16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, to_device(a), d_coef,
+                                                                 d_flags, st, flat_out, a0);
     return cudaGetLastError();
 }
 
-cudaError_t zsl_partition(const ZsTile *d_tiles, int64_t ntiles, const float *W,
+cudaError_t zsl_partition(const ZsTile *d_tiles, int64_t ntiles, int dtype, const float *W,
                           const zs_shard_state &st, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
-    partition_kernel<<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, W, st);
+    if (dtype == ZS_DTYPE_FP16)
+        partition_kernel<FP16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, W, st);
+    else
+        partition_kernel<BF16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, W, st);
     return cudaGetLastError();
 }
