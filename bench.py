@@ -72,6 +72,8 @@ class DeviceWorkload:
         cfg.reduce_bucket_size = w.reduce_bucket_size
         cfg.prefetch_bucket_size = w.prefetch_bucket_size
         cfg.sub_group_size = w.sub_group_size
+        self.fp16 = w.dtype == "fp16"
+        cfg.dtype = zs.ZS_DTYPE_FP16 if self.fp16 else zs.ZS_DTYPE_BF16
         self.plan = zs.zs_build_partition(cfg, w.numel, w.ds_id)
         info = self.info = zs.zs_plan_info(self.plan)
         N, S, Pn = info["n_ranks"], info["shard_elems"], info["persist_elems"]
@@ -94,6 +96,10 @@ class DeviceWorkload:
         self.flat = E(info["flat_elems"], torch.int16)
         self.hp = w.hparams()
         self.t = 0
+        # fp16: device-resident dynamic loss scale
+        self.d_scale = torch.tensor([w.loss_scale, 0, 0, 0], dtype=torch.float32, device=self.dev)
+        self.d_good = torch.zeros(4, dtype=torch.int32, device=self.dev)
+        self.scaler = zs.make_loss_scaler(self.d_scale, self.d_good, 2.0, 1.0, w.scale_window)
         # weights: full fp32 parameters from the generator, partitioned once
         W = E(info["psi"], torch.float32)
         sg.fill_weight_f32(W, 0, self.seed, w.weight_sigma)
@@ -113,7 +119,11 @@ class DeviceWorkload:
         if total and pool_elems < total:
             pool_elems = max(pool_elems, need)
         self.pool = E(pool_elems, torch.int16)
-        sg.fill_grad_bf16(self.pool, 0, self.seed, w.grad_sigma, w.outlier_frac, w.outlier_scale)
+        if self.fp16:
+            sg.fill_grad_fp16(self.pool, 0, self.seed, w.fp16_log2_scale)
+        else:
+            sg.fill_grad_bf16(self.pool, 0, self.seed, w.grad_sigma, w.outlier_frac,
+                              w.outlier_scale)
         self.pool_elems = self.pool.numel()
         self.offs = wl.pool_offsets(self.buf_elems, N, self.pool_elems) if nb else []
         base = self.pool.data_ptr()
@@ -128,9 +138,23 @@ class DeviceWorkload:
 
     def step(self, stream=None):
         self.t += 1
+        if self.fp16:
+            self.zs.zs_shard_step_scaled(self.plan, self.ptr_table, self.state, self.scratch,
+                                         self.hp, self.t, self.max_norm, self.scaler, self.d_norm,
+                                         self.d_coef, self.d_flags, self.flat, stream)
+            return
         self.zs.zs_shard_step(self.plan, self.ptr_table, self.state, self.scratch, self.hp, self.t,
                               self.max_norm, self.d_norm, self.d_coef, self.d_flags, self.flat,
                               stream)
+
+    def norm(self, recompute=False):
+        if self.fp16:
+            self.zs.zs_unscale_and_clip(self.plan, self.gs, self.gP, self.scratch, recompute,
+                                        self.max_norm, self.scaler, self.d_norm, self.d_coef,
+                                        self.d_flags)
+        else:
+            self.zs.zs_grad_norm(self.plan, self.gs, self.gP, self.scratch, recompute,
+                                 self.max_norm, self.d_norm, self.d_coef, self.d_flags)
 
     def step_timed(self, ev):
         """The same step as step(), as its three calls with events between."""
@@ -139,8 +163,7 @@ class DeviceWorkload:
         ev[0].record()
         zs.zs_reduce_scatter_all(self.plan, self.ptr_table, self.gs, self.gP, self.scratch)
         ev[1].record()
-        zs.zs_grad_norm(self.plan, self.gs, self.gP, self.scratch, False, self.max_norm,
-                        self.d_norm, self.d_coef, self.d_flags)
+        self.norm()
         ev[2].record()
         zs.zs_adam_gather(self.plan, self.hp, self.t, self.d_coef, self.d_flags, self.state,
                           self.flat)
@@ -163,8 +186,7 @@ class DeviceWorkload:
         self.t += 1
         for b, ptrs in enumerate(self._bptrs):
             zs.zs_reduce_scatter(self.plan, b, ptrs, self.gs, self.gP, self.scratch)
-        zs.zs_grad_norm(self.plan, self.gs, self.gP, self.scratch, False, self.max_norm,
-                        self.d_norm, self.d_coef, self.d_flags)
+        self.norm()
         for sg in range(self.info["n_sub_groups"]):
             zs.zs_adam_step(self.plan, sg, self.hp, self.t, self.d_coef, self.d_flags, self.state)
         launches = len(self._bptrs) + 2 + self.info["n_sub_groups"]
@@ -411,8 +433,7 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
             ptrs = [base + 2 * k * _align8(dw.buf_elems[b]) for k in range(N)]
             zs.zs_reduce_scatter(dw.plan, b, ptrs, dw.gs, dw.gP, dw.scratch)
             free[s].record(comp)
-        zs.zs_grad_norm(dw.plan, dw.gs, dw.gP, dw.scratch, False, dw.max_norm, dw.d_norm,
-                        dw.d_coef, dw.d_flags)
+        dw.norm()
         zs.zs_adam_gather(dw.plan, dw.hp, dw.t, dw.d_coef, dw.d_flags, dw.state, dw.flat)
         out[0:1].copy_(dw.d_norm[0:1].view(torch.int32), non_blocking=True)
         out[1:2].copy_(dw.d_flags[0:1], non_blocking=True)
@@ -476,9 +497,9 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "storage": "bf16 gradients and parameters, f32 master / exp_avg / exp_avg_sq",
+        "storage": f"{w.dtype} gradients and parameters, f32 master / exp_avg / exp_avg_sq",
         "data": "synthetic (Philox4x32-10 gradients and weights; architecture shapes only)",
-        "config": {"workload": w.name, "n_ranks": w.n_ranks, "psi": psi,
+        "config": {"workload": w.name, "n_ranks": w.n_ranks, "psi": psi, "storage_dtype": w.dtype,
                    "n_params": w.n_params, "reduce_bucket_size": w.reduce_bucket_size,
                    "prefetch_bucket_size": w.prefetch_bucket_size,
                    "param_persistence_threshold": w.persistence_threshold,

@@ -40,6 +40,10 @@ class Workload:
     max_norm: float = 1.0
     seed: int = 0x5EED
     ds_id: list = field(default=None)
+    dtype: str = "bf16"             # 16-bit storage: "bf16" | "fp16"
+    fp16_log2_scale: int = -2       # fp16 gradients: floor(z/512) * 2^e (std ~52 = 1e-3 * 2^16)
+    loss_scale: float = 65536.0     # fp16: initial dynamic loss scale
+    scale_window: int = 1000
 
     @property
     def numel(self) -> list:
@@ -164,6 +168,14 @@ def llama3_attn() -> Workload:
                     grad_sigma=1e-3, steps=1, max_norm=1.0, seed=0x5EED0006)
 
 
+def llama3_8b_fp16() -> Workload:
+    """The Llama-3-8B-shaped list with fp16 gradients and parameters, the
+    gradients scaled by a dynamic loss scale starting at 2^16."""
+    w = llama3_8b()
+    w.name, w.dtype, w.seed = "llama3_8b_fp16", "fp16", 0x5EED0007
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama_layer": llama_layer,
@@ -171,6 +183,7 @@ WORKLOADS = {
     "llama3_16_layers": llama3_layers,
     "llama3_8b": llama3_8b,
     "llama3_attn": llama3_attn,
+    "llama3_8b_fp16": llama3_8b_fp16,
 }
 
 

@@ -33,7 +33,13 @@ def _oracle_plan(w):
     return oplan.build_partition(w.numel, w.n_ranks, threshold=w.persistence_threshold,
                                  reduce_bucket_size=w.reduce_bucket_size,
                                  prefetch_bucket_size=w.prefetch_bucket_size,
-                                 sub_group_size=w.sub_group_size, ds_id=w.ds_id)
+                                 sub_group_size=w.sub_group_size, ds_id=w.ds_id, dtype=w.dtype)
+
+
+def _grads(w, idx):
+    if w.dtype == "fp16":
+        return philox.grad_fp16(w.seed, 0, idx, w.fp16_log2_scale)
+    return philox.grad_bf16(w.seed, 0, idx, w.grad_sigma, w.outlier_frac, w.outlier_scale)
 
 
 def _samples(op, rng, n_random=3000):
@@ -83,7 +89,8 @@ def _locate(op, w, dw, cols, ranks):
     return kind, win, pool_idx
 
 
-@pytest.mark.parametrize("name", ["llama_layer", "many_small", "llama3_16_layers", "llama3_8b"])
+@pytest.mark.parametrize("name", ["llama_layer", "many_small", "llama3_16_layers", "llama3_8b",
+                                  "llama3_8b_fp16"])
 def test_fullsize_sampled(name):
     w = workloads.WORKLOADS[name]()
     op = _oracle_plan(w)
@@ -92,7 +99,10 @@ def test_fullsize_sampled(name):
         assert dw.info["shard_elems"] == op.S and dw.info["flat_elems"] == op.flat_elems
         dw.step()
         torch.cuda.synchronize()
-        assert int(dw.d_flags[0]) == 0 and float(dw.d_coef[0]) == 1.0
+        # max_norm = 0: no clipping, the coefficient is 1 / loss scale (1 for bf16)
+        S = np.float32(w.loss_scale if w.dtype == "fp16" else 1.0)
+        coef = np.float32(1.0) / S
+        assert int(dw.d_flags[0]) == 0 and float(dw.d_coef[0]) == float(coef)
         rng = np.random.default_rng(11)
         ranks, cols = _samples(op, rng)
         idx = torch.from_numpy(ranks * op.S + cols).to(dw.dev)
@@ -100,18 +110,20 @@ def test_fullsize_sampled(name):
                for k, a in [("gs", "gs"), ("ps", "ps"), ("p", "master"), ("m", "m"), ("v", "v")]}
         kind, win, pidx = _locate(op, w, dw, cols, ranks)
         data = kind == 0
-        vals = philox.grad_bf16(w.seed, 0, pidx[:, data].ravel(), w.grad_sigma, w.outlier_frac,
-                                w.outlier_scale).reshape(op.n_ranks, -1)
-        gs_ref = ostep.reduce_mean_bf16(vals)
+        vals = _grads(w, pidx[:, data].ravel()).reshape(op.n_ranks, -1)
+        gs_ref = ostep.reduce_mean(vals, w.dtype)
         W = philox.weight_f32(w.seed, win[data].astype(np.uint64), w.weight_sigma)
         z = np.zeros_like(W)
-        p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, np.float32(1.0),
-                                           ostep.adam_consts(w.hparams(), 1))
+        p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, coef,
+                                           ostep.adam_consts(w.hparams(), 1), w.dtype)
         assert np.array_equal(got["gs"].view(np.uint16)[data], gs_ref)
         H.assert_f32_close(got["p"][data], p1, "master")
         H.assert_f32_close(got["m"][data], m1, "exp_avg")
         H.assert_f32_close(got["v"][data], v1, "exp_avg_sq")
-        H.assert_bf16_within_ulp(got["ps"].view(np.uint16)[data], pb, "param_shards")
+        if w.dtype == "fp16":
+            H.assert_fp16_within_ulp(got["ps"].view(np.uint16)[data], pb, "param_shards")
+        else:
+            H.assert_bf16_within_ulp(got["ps"].view(np.uint16)[data], pb, "param_shards")
         # padding and alignment columns stay exactly zero
         for k in ("gs", "ps", "p", "m", "v"):
             assert not np.any(got[k].view(np.uint8).reshape(len(cols), -1)[~data])
@@ -138,23 +150,23 @@ def test_fullsize_sampled(name):
                     ents.append((p.persist_off + e, p.input_off + e,
                                  [dw.offs[b][q] + ent.buf_off + e for q in range(op.n_ranks)]))
             pidx2 = torch.tensor([x[0] for x in ents], device=dw.dev)
-            pv = philox.grad_bf16(w.seed, 0, np.array([x[2] for x in ents], dtype=np.uint64).T.ravel(),
-                                  w.grad_sigma, w.outlier_frac, w.outlier_scale).reshape(op.n_ranks, -1)
-            gP_ref = ostep.reduce_mean_bf16(pv)
+            pv = _grads(w, np.array([x[2] for x in ents], dtype=np.uint64).T.ravel()
+                        ).reshape(op.n_ranks, -1)
+            gP_ref = ostep.reduce_mean(pv, w.dtype)
             assert np.array_equal(dw.gP.index_select(0, pidx2).cpu().numpy().view(np.uint16), gP_ref)
             Wp = philox.weight_f32(w.seed, np.array([x[1] for x in ents], dtype=np.uint64),
                                    w.weight_sigma)
             zp = np.zeros_like(Wp)
-            pp1 = ostep.adam_update(Wp, zp, zp, gP_ref, np.float32(1.0),
-                                    ostep.adam_consts(w.hparams(), 1))[0]
+            pp1 = ostep.adam_update(Wp, zp, zp, gP_ref, coef,
+                                    ostep.adam_consts(w.hparams(), 1), w.dtype)[0]
             H.assert_f32_close(dw.pm.index_select(0, pidx2).cpu().numpy(), pp1, "p_master")
         # the norm is the norm of the reduced-gradient buffers
         tot = 0.0
         for buf, n in ((dw.gs, op.n_ranks * op.S), (dw.gP, op.Pn_alloc)):
             for ch in buf[:n].split(1 << 27):
-                x = ch.view(torch.bfloat16).double()
+                x = ch.view(torch.float16 if w.dtype == "fp16" else torch.bfloat16).double()
                 tot += float((x * x).sum())
-        ref = float(np.sqrt(tot))
+        ref = float(np.sqrt(tot)) / float(S)
         assert abs(float(dw.d_norm[0]) - ref) <= 1e-5 * ref
     finally:
         del dw
