@@ -532,6 +532,23 @@ def run_gpu(args):
                       "launches_per_step": n_unfused,
                       "calls": "zs_reduce_scatter per bucket, zs_grad_norm, zs_adam_step per "
                                "sub-group, zs_all_gather_coalesced per gather bucket"}
+    # ZeRO-2 residency: no shard buffer, the parameters live in the replica
+    st2 = dw.zs.make_state(grad_shards=dw.gs, param_shards=None, master=dw.master, exp_avg=dw.m,
+                           exp_avg_sq=dw.v, persist_grads=dw.gP, persist_params=dw.pP,
+                           p_master=dw.pm, p_exp_avg=dw.pmm, p_exp_avg_sq=dw.pmv)
+    state3, dw.state = dw.state, st2
+    dw.step()
+    torch.cuda.synchronize(dev)
+    u0.record()
+    for _ in range(KU):
+        dw.step()
+    u1.record()
+    torch.cuda.synchronize(dev)
+    dw.state = state3
+    z2 = u0.elapsed_time(u1) / KU
+    res["zero2"] = {"ms_per_step": z2, "params_per_s": psi / (z2 * 1e-3),
+                    "alg_bytes_per_elem": 2 * dw.N + 30,
+                    "note": "same fused step, parameters kept only in the full replica"}
     if not args.no_e2e:
         res["e2e"] = run_e2e(dw, steps=args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -386,8 +386,15 @@ zs_status zs_reduce_scatter_all(const zs_plan *plan, const void *const *d_rank_g
  * bf16 cast of every element (all sub-groups), and each new bf16 parameter
  * also written at its place in model flat space (flat_out, flat_elems,
  * 2-byte aligned), as zs_all_gather_coalesced of every gather bucket would.
- * Same arguments and skip rule as zs_adam_step.  Errors: ZS_EINVAL,
- * ZS_ESTATE, ZS_ECUDA. */
+ * Same arguments and skip rule as zs_adam_step.
+ * ZeRO-1/2 residency ([Core flow] §4 table: stages 1 and 2 keep the full
+ * parameters on every rank; [ZeRO-3 chapter] §1): st->param_shards may be
+ * NULL, and then the new parameters are written only to flat_out, the full
+ * replica (a rank's shard is a slice of it), saving the shard write;
+ * zs_shard_step and zs_shard_step_scaled accept the same.  ZeRO-1's
+ * gradient all-reduce is zs_reduce_scatter followed by
+ * zs_all_gather_coalesced over grad_shards.  Errors: ZS_EINVAL, ZS_ESTATE,
+ * ZS_ECUDA. */
 zs_status zs_adam_gather(const zs_plan *plan, const zs_adam_hparams *hp, int64_t step,
                          const float *d_clip_coef, const int32_t *d_flags,
                          const zs_shard_state *st, void *flat_out, void *stream);

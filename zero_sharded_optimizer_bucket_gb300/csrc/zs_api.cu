@@ -27,13 +27,14 @@ zs_status need_table(const zs_plan *P, const char *fn) {
 // Pointers of the spaces a call touches: shard arrays when N*S > 0,
 // persistent arrays when Pn > 0.
 zs_status check_state(const zs_plan *P, const zs_shard_state *st, bool grads, bool update,
-                      const char *fn) {
+                      const char *fn, bool shards_optional = false) {
     if (!st) return zs_fail(ZS_EINVAL, "%s: NULL state", fn);
     const bool shard = P->S > 0, pers = P->Pn_alloc > 0;
     struct Item { const void *p; bool used; const char *name; };
     const Item items[] = {
         {st->grad_shards, shard && grads, "grad_shards"},
-        {st->param_shards, shard && update, "param_shards"},
+        {st->param_shards, shard && update && !(shards_optional && !st->param_shards),
+         "param_shards"},
         {st->master, shard && update, "master"},
         {st->exp_avg, shard && update, "exp_avg"},
         {st->exp_avg_sq, shard && update, "exp_avg_sq"},
@@ -327,7 +328,7 @@ zs_status zs_adam_gather(const zs_plan *P, const zs_adam_hparams *hp, int64_t st
     if (r) return r;
     ZsAdamScalars c;
     if ((r = adam_scalars(hp, step, &c, fn))) return r;
-    if ((r = check_state(P, st, true, true, fn))) return r;
+    if ((r = check_state(P, st, true, true, fn, true))) return r;
     if (!al(d_clip_coef, 4) || !al(d_flags, 4))
         return zs_fail(ZS_EINVAL, "%s: d_clip_coef / d_flags NULL or misaligned", fn);
     if (P->flat_elems > 0 && !al(flat_out, 2))
@@ -345,7 +346,7 @@ zs_status zs_shard_step(const zs_plan *P, const void *const *d_rank_grads,
     if (r) return r;
     ZsAdamScalars c;
     if ((r = adam_scalars(hp, step, &c, fn))) return r;
-    if ((r = check_state(P, st, true, true, fn))) return r;
+    if ((r = check_state(P, st, true, true, fn, true))) return r;
     if ((r = check_scratch(P, norm_scratch, fn))) return r;
     if ((r = check_scalars(d_norm, d_clip_coef, d_flags, fn))) return r;
     if (P->flat_elems > 0 && !al(flat_out, 2))
@@ -369,7 +370,7 @@ zs_status zs_shard_step_scaled(const zs_plan *P, const void *const *d_rank_grads
     if (r) return r;
     ZsAdamScalars c;
     if ((r = adam_scalars(hp, step, &c, fn))) return r;
-    if ((r = check_state(P, st, true, true, fn))) return r;
+    if ((r = check_state(P, st, true, true, fn, true))) return r;
     if ((r = check_scratch(P, norm_scratch, fn))) return r;
     if ((r = check_scalars(d_norm, d_clip_coef, d_flags, fn))) return r;
     if (!scaler || !al(scaler->d_scale, 4) || scaler->reserved != 0 ||

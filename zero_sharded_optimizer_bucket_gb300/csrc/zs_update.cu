@@ -63,7 +63,8 @@ __device__ __forceinline__ void adam8(const StatePtrs &s, int64_t off, float coe
     store8f(s.p + off, p);
     store8f(s.m + off, m);
     store8f(s.v + off, v);
-    *reinterpret_cast<uint4 *>(s.param + off) = pack8(r);
+    // no shard buffer: the parameters live only in the gathered replica
+    if (s.param) *reinterpret_cast<uint4 *>(s.param + off) = pack8(r);
 }
 
 template <class T>
@@ -75,7 +76,7 @@ __device__ __forceinline__ uint32_t adam1(const StatePtrs &s, int64_t x, float c
     s.p[x] = p;
     s.m[x] = m;
     s.v[x] = v;
-    s.param[x] = (uint16_t)r;
+    if (s.param) s.param[x] = (uint16_t)r;
     return r;
 }
 
