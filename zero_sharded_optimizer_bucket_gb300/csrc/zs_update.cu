@@ -47,7 +47,7 @@ __device__ __forceinline__ void store8f(float *a, const float o[8]) {
 }
 
 // 8 aligned elements at off: Adam on all of them, bf16 results in r.
-template <class T>
+template <class T, bool SHARD = true>
 __device__ __forceinline__ void adam8(const StatePtrs &s, int64_t off, float coef, const AdamC &c,
                                       uint32_t r[8]) {
     const uint4 gv = ldg16(s.g + off);
@@ -63,11 +63,11 @@ __device__ __forceinline__ void adam8(const StatePtrs &s, int64_t off, float coe
     store8f(s.p + off, p);
     store8f(s.m + off, m);
     store8f(s.v + off, v);
-    // no shard buffer: the parameters live only in the gathered replica
-    if (s.param) *reinterpret_cast<uint4 *>(s.param + off) = pack8(r);
+    // SHARD false: no shard buffer, the parameters live only in the replica
+    if (SHARD) *reinterpret_cast<uint4 *>(s.param + off) = pack8(r);
 }
 
-template <class T>
+template <class T, bool SHARD = true>
 __device__ __forceinline__ uint32_t adam1(const StatePtrs &s, int64_t x, float coef,
                                           const AdamC &c) {
     float p = s.p[x], m = s.m[x], v = s.v[x];
@@ -76,7 +76,7 @@ __device__ __forceinline__ uint32_t adam1(const StatePtrs &s, int64_t x, float c
     s.p[x] = p;
     s.m[x] = m;
     s.v[x] = v;
-    if (s.param) s.param[x] = (uint16_t)r;
+    if (SHARD) s.param[x] = (uint16_t)r;
     return r;
 }
 
@@ -103,7 +103,7 @@ adam_kernel(int N, int64_t S, int64_t s_lo, int64_t W, int64_t p_lo, int64_t PW,
 // Fused pass 2: Adam + cast on one tile, and the cast parameters also
 // written at their place in model flat space (the all-gather of the next
 // forward pass, [ZeRO-3 chapter] §5.2), straight from registers.
-template <class T>
+template <class T, bool SHARD>
 __global__ void __launch_bounds__(THREADS)
 step2_kernel(const ZsTile *__restrict__ tiles, AdamC c, const float *__restrict__ d_coef,
              const int32_t *__restrict__ d_flags, zs_shard_state st,
@@ -127,12 +127,17 @@ step2_kernel(const ZsTile *__restrict__ tiles, AdamC c, const float *__restrict_
 #pragma unroll
         for (int i = 0; i < 8; ++i) r[i] = 0u;
         if (act) {
+            // persistent parameters are always stored whole; shard tiles
+            // skip the shard store when SHARD is false (tile-uniform branch)
             if (x0 >= D && x0 + 8 <= D + L) {
-                adam8<T>(s, x0, coef, c, r);
+                if (pers) adam8<T, true>(s, x0, coef, c, r);
+                else adam8<T, SHARD>(s, x0, coef, c, r);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (x0 + i >= D && x0 + i < D + L) r[i] = adam1<T>(s, x0 + i, coef, c);
+                    if (x0 + i >= D && x0 + i < D + L)
+                        r[i] = pers ? adam1<T, true>(s, x0 + i, coef, c)
+                                    : adam1<T, SHARD>(s, x0 + i, coef, c);
             }
         }
         if (pers) continue;
@@ -251,12 +256,15 @@ cudaError_t zsl_step2(const ZsTile *d_tiles, int64_t ntiles, int dtype, const Zs
                       uint16_t *flat_out, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     const int a0 = (int)((reinterpret_cast<uintptr_t>(flat_out) >> 1) & 7);
-    if (dtype == ZS_DTYPE_FP16)
-        step2_kernel<FP16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, to_device(a), d_coef,
-                                                                 d_flags, st, flat_out, a0);
-    else
-        step2_kernel<BF16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, to_device(a), d_coef,
-                                                                 d_flags, st, flat_out, a0);
+    const dim3 g((unsigned)ntiles), b(THREADS);
+    const AdamC c = to_device(a);
+    if (dtype == ZS_DTYPE_FP16) {
+        if (st.param_shards) step2_kernel<FP16T, true><<<g, b, 0, s>>>(d_tiles, c, d_coef, d_flags, st, flat_out, a0);
+        else step2_kernel<FP16T, false><<<g, b, 0, s>>>(d_tiles, c, d_coef, d_flags, st, flat_out, a0);
+    } else {
+        if (st.param_shards) step2_kernel<BF16T, true><<<g, b, 0, s>>>(d_tiles, c, d_coef, d_flags, st, flat_out, a0);
+        else step2_kernel<BF16T, false><<<g, b, 0, s>>>(d_tiles, c, d_coef, d_flags, st, flat_out, a0);
+    }
     return cudaGetLastError();
 }
 
