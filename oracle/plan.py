@@ -39,6 +39,12 @@ Definitions (each a reading of the pages; the design notes list them):
 * Sub-groups.  All parameters in ds_id order, weighted by their per-rank
   footprint (ps for a partitioned, numel for a persistent parameter), closed
   when the next would exceed sub_group_size (1e9, [ZeRO-3 chapter] §6.1).
+* HSDP.  With shard_group_size G (a divisor of N; default N) the N ranks
+  form N/G replica groups of G consecutive ranks: parameters are
+  partitioned over the G ranks of a group, the groups hold identical
+  replicas ([Core flow] §4: FSDP inside a group, DDP across groups).  Every
+  layout above then uses G in place of N; the gradient mean still runs over
+  all N ranks (see step.reduce_scatter).
 """
 from __future__ import annotations
 
@@ -96,7 +102,8 @@ class GatherBucket:
 
 @dataclass
 class Plan:
-    n_ranks: int
+    n_ranks: int            # N: ranks that contribute gradients
+    group: int              # G: ranks a parameter is partitioned over (N unless HSDP)
     dtype: str              # 16-bit storage of gradients and parameters: "bf16" | "fp16"
     threshold: int
     reduce_bucket_size: int
@@ -130,7 +137,7 @@ def build_partition(numel, n_ranks: int, threshold: int = 100_000,
                     reduce_bucket_size: int = 5_000_000,
                     prefetch_bucket_size: int = 50_000_000,
                     sub_group_size: int = 1_000_000_000, ds_id=None,
-                    dtype: str = "bf16") -> Plan:
+                    dtype: str = "bf16", shard_group_size: int = None) -> Plan:
     numel = [int(x) for x in numel]
     n = len(numel)
     if n_ranks < 1:
@@ -147,7 +154,10 @@ def build_partition(numel, n_ranks: int, threshold: int = 100_000,
     if len(set(ds_id)) != n:
         raise ValueError("ds_id must be unique")
     order = sorted(range(n), key=lambda i: ds_id[i])
-    N = n_ranks
+    group = n_ranks if not shard_group_size else int(shard_group_size)
+    if group < 1 or n_ranks % group:
+        raise ValueError("shard_group_size must divide n_ranks")
+    N = group      # every layout below is over the shard owners of a group
     params = [Param(index=i, ds_id=ds_id[i], numel=numel[i],
                     persistent=numel[i] < threshold) for i in range(n)]
 
@@ -251,7 +261,7 @@ def build_partition(numel, n_ranks: int, threshold: int = 100_000,
                 s_cur = p.shard_off + _align8(p.ps)
         sub_groups.append(SubGroup(ids, s_lo, s_cur, p_lo, p_cur))
 
-    return Plan(n_ranks=N, dtype=dtype, threshold=threshold, reduce_bucket_size=B,
+    return Plan(n_ranks=n_ranks, group=group, dtype=dtype, threshold=threshold, reduce_bucket_size=B,
                 prefetch_bucket_size=G, sub_group_size=U, params=params,
                 order=order, S=s_run, S_logical=S_logical, Pn_alloc=p_run, Pn=Pn,
                 psi=sum(numel), flat_elems=f_run, input_elems=w_run,

@@ -46,7 +46,7 @@ class State:
 
 
 def new_state(plan: Plan) -> State:
-    N, S, P = plan.n_ranks, plan.S, plan.Pn_alloc
+    N, S, P = plan.group, plan.S, plan.Pn_alloc
     z32 = lambda *s: np.zeros(s, dtype=np.float32)
     z16 = lambda *s: np.zeros(s, dtype=np.uint16)
     return State(z32(N, S), z32(N, S), z32(N, S), z16(N, S), z16(N, S),
@@ -63,7 +63,7 @@ def partition(plan: Plan, W: np.ndarray) -> State:
     is the rounded master."""
     W = np.asarray(W, dtype=np.float32)
     st = new_state(plan)
-    N = plan.n_ranks
+    N = plan.group
     for p in plan.params:
         if p.persistent:
             st.p_master[p.persist_off:p.persist_off + p.numel] = \
@@ -110,12 +110,31 @@ def reduce_mean(vals, dtype: str = "bf16") -> np.ndarray:
     return reduce_mean_bf16(vals) if dtype == "bf16" else reduce_mean_fp16(vals)
 
 
+def reduce_mean_groups(vals, G: int, dtype: str = "bf16") -> np.ndarray:
+    """HSDP mean ([Core flow] §4: reduce-scatter inside each replica group,
+    all-reduce across groups): each group's G ranks are summed in rank order
+    from 0 (float32), the group sums are added in group order from 0, and
+    the total is divided by the number of ranks N and rounded to 16 bits.
+    With one group this is the flat mean, bit for bit (0 + s == s)."""
+    vals = np.asarray(vals, dtype=np.uint16)
+    N = vals.shape[0]
+    if G == N:
+        return reduce_mean(vals, dtype)
+    total = np.zeros(vals.shape[1:], dtype=np.float32)
+    for g in range(N // G):
+        inner = np.zeros(vals.shape[1:], dtype=np.float32)
+        for j in range(G):
+            inner = inner + to_f32(vals[g * G + j], dtype)
+        total = total + inner
+    return from_f32(total / F32(N), dtype)
+
+
 def reduce_scatter(plan: Plan, bucket: int, rank_bufs, st: State) -> None:
     """Reduce bucket `bucket` of all N ranks and keep each rank's slice
     ([ZeRO-3 chapter] §6.2: all_reduce of the bucket then each rank keeps its
     range, or reduce_scatter to the owners; both give this result).
     rank_bufs[k] is rank k's gradient buffer of the bucket (uint16)."""
-    N = plan.n_ranks
+    N, G = plan.n_ranks, plan.group
     assert len(rank_bufs) == N
     for ent in plan.reduce_buckets[bucket]:
         p = plan.params[ent.param]
@@ -123,11 +142,11 @@ def reduce_scatter(plan: Plan, bucket: int, rank_bufs, st: State) -> None:
             L = ent.e_hi - ent.e_lo
             vals = np.stack([np.asarray(b[ent.buf_off:ent.buf_off + L]) for b in rank_bufs])
             st.persist_grads[p.persist_off + ent.e_lo:p.persist_off + ent.e_hi] = \
-                reduce_mean(vals, plan.dtype)
+                reduce_mean_groups(vals, G, plan.dtype)
             continue
         # the bucket holding the parameter's last element also owns the
         # padding elements numel .. N*ps-1 (gradient zero)
-        hi = N * p.ps if ent.e_hi == p.numel else ent.e_hi
+        hi = G * p.ps if ent.e_hi == p.numel else ent.e_hi
         if hi <= ent.e_lo:
             continue
         e = np.arange(ent.e_lo, hi)
@@ -136,7 +155,7 @@ def reduce_scatter(plan: Plan, bucket: int, rank_bufs, st: State) -> None:
         src = ent.buf_off + (e[valid] - ent.e_lo)
         for k in range(N):
             vals[k, valid] = np.asarray(rank_bufs[k])[src]
-        st.grad_shards[e // p.ps, p.shard_off + e % p.ps] = reduce_mean(vals, plan.dtype)
+        st.grad_shards[e // p.ps, p.shard_off + e % p.ps] = reduce_mean_groups(vals, G, plan.dtype)
 
 
 # ---------------------------------------------------------------- A3 -----
@@ -310,7 +329,7 @@ def all_gather_coalesced(plan: Plan, params, param_shards: np.ndarray):
     params = [int(i) for i in params]
     if len(set(params)) != len(params):
         raise ValueError("duplicate parameter in gather list")
-    N = plan.n_ranks
+    N = plan.group
     srt = sorted(params, key=lambda i: plan.params[i].ds_id)
     offs, off = {}, 0
     for i in srt:
