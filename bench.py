@@ -74,15 +74,17 @@ class DeviceWorkload:
         cfg.sub_group_size = w.sub_group_size
         self.fp16 = w.dtype == "fp16"
         cfg.dtype = zs.ZS_DTYPE_FP16 if self.fp16 else zs.ZS_DTYPE_BF16
+        cfg.shard_group_size = w.shard_group_size
         self.plan = zs.zs_build_partition(cfg, w.numel, w.ds_id)
         info = self.info = zs.zs_plan_info(self.plan)
         N, S, Pn = info["n_ranks"], info["shard_elems"], info["persist_elems"]
         self.N = N
+        R = info["shard_group_size"]     # rows of shard space (N unless HSDP)
         E = lambda n, dt: torch.empty(max(int(n), 8), dtype=dt, device=self.dev)
         self.table = E(info["device_table_bytes"], torch.uint8)
         zs.zs_plan_upload(self.plan, self.table, self.table.numel())
-        self.gs, self.ps = E(N * S, torch.int16), E(N * S, torch.int16)
-        self.master, self.m, self.v = (E(N * S, torch.float32) for _ in range(3))
+        self.gs, self.ps = E(R * S, torch.int16), E(R * S, torch.int16)
+        self.master, self.m, self.v = (E(R * S, torch.float32) for _ in range(3))
         self.gP, self.pP = E(Pn, torch.int16), E(Pn, torch.int16)
         self.pm, self.pmm, self.pmv = (E(Pn, torch.float32) for _ in range(3))
         self.state = zs.make_state(grad_shards=self.gs, param_shards=self.ps, master=self.master,
@@ -500,6 +502,7 @@ def run_gpu(args):
         "storage": f"{w.dtype} gradients and parameters, f32 master / exp_avg / exp_avg_sq",
         "data": "synthetic (Philox4x32-10 gradients and weights; architecture shapes only)",
         "config": {"workload": w.name, "n_ranks": w.n_ranks, "psi": psi, "storage_dtype": w.dtype,
+                   "shard_group_size": dw.info["shard_group_size"],
                    "n_params": w.n_params, "reduce_bucket_size": w.reduce_bucket_size,
                    "prefetch_bucket_size": w.prefetch_bucket_size,
                    "param_persistence_threshold": w.persistence_threshold,

@@ -100,6 +100,15 @@ typedef struct {
     int64_t reduce_bucket_size;           /* elements, >= 1                      */
     int64_t prefetch_bucket_size;         /* elements, >= 1 (gather buckets)     */
     int64_t sub_group_size;               /* per-rank elements, >= 1             */
+    /* HSDP ([Core flow] §4: FSDP inside a group, DDP across groups): the N
+     * ranks form N/G replica groups of G consecutive ranks; parameters are
+     * partitioned over the G ranks of a group (every layout below then uses
+     * G where it says N) and the groups hold identical replicas, stored
+     * once.  The gradient mean sums each group's ranks in rank order, then
+     * the group sums in group order, and divides by N.  0 or N: plain ZeRO-3
+     * (bit-identical to it).  Must divide N. */
+    int32_t shard_group_size;
+    int32_t reserved;                     /* must be 0                           */
 } zs_config;
 
 typedef struct {
@@ -112,6 +121,7 @@ typedef struct {
     int32_t n_ranks, n_params;
     int32_t n_reduce_buckets, n_gather_buckets;
     int32_t n_sub_groups, dtype;
+    int32_t shard_group_size, reserved;   /* G (N unless HSDP)                      */
     int64_t psi;                    /* sum of numel                                   */
     int64_t shard_elems;            /* S: length of one shard row (multiple of 8)     */
     int64_t shard_elems_logical;    /* sum of ps over partitioned parameters          */

@@ -44,6 +44,7 @@ class Workload:
     fp16_log2_scale: int = -2       # fp16 gradients: floor(z/512) * 2^e (std ~52 = 1e-3 * 2^16)
     loss_scale: float = 65536.0     # fp16: initial dynamic loss scale
     scale_window: int = 1000
+    shard_group_size: int = 0       # HSDP group size G (0: plain ZeRO-3 over all N)
 
     @property
     def numel(self) -> list:
@@ -176,6 +177,14 @@ def llama3_8b_fp16() -> Workload:
     return w
 
 
+def llama3_8b_hsdp() -> Workload:
+    """The Llama-3-8B-shaped list, N=16 ranks as 2 replica groups of 8
+    (HSDP: shard within a group, replicate across groups)."""
+    w = llama3_8b()
+    w.name, w.shard_group_size, w.seed = "llama3_8b_hsdp", 8, 0x5EED0008
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama_layer": llama_layer,
@@ -184,6 +193,7 @@ WORKLOADS = {
     "llama3_8b": llama3_8b,
     "llama3_attn": llama3_attn,
     "llama3_8b_fp16": llama3_8b_fp16,
+    "llama3_8b_hsdp": llama3_8b_hsdp,
 }
 
 

@@ -70,15 +70,16 @@ class Guarded:
 class DevicePlan:
     def __init__(self, numel, N, threshold=100_000, B=5_000_000, G=50_000_000, U=10**9,
                  ds_id=None, seed=1234, sigma=1e-2, outlier=0.0, device="cuda:0", dtype="bf16",
-                 log2_scale=-4, outlier_log2=0):
+                 log2_scale=-4, outlier_log2=0, group=0):
         self.dev = torch.device(device)
         self.numel, self.N, self.seed, self.sigma, self.outlier = numel, N, seed, sigma, outlier
         self.dtype, self.log2_scale, self.outlier_log2 = dtype, log2_scale, outlier_log2
         self.op = oplan.build_partition(numel, N, threshold=threshold, reduce_bucket_size=B,
                                         prefetch_bucket_size=G, sub_group_size=U, ds_id=ds_id,
-                                        dtype=dtype)
+                                        dtype=dtype, shard_group_size=group or None)
         cfg = zs.zs_default_config(N)
         cfg.dtype = zs.ZS_DTYPE_FP16 if dtype == "fp16" else zs.ZS_DTYPE_BF16
+        cfg.shard_group_size = group
         cfg.param_persistence_threshold = threshold
         cfg.reduce_bucket_size = B
         cfg.prefetch_bucket_size = G
@@ -87,6 +88,7 @@ class DevicePlan:
         self.info = zs.zs_plan_info(self.plan)
         assert self.info["shard_elems"] == self.op.S and self.info["persist_elems"] == self.op.Pn_alloc
         S, P = self.op.S, self.op.Pn_alloc
+        N = self.op.group          # rows of shard space: a group's shard owners
         d = self.dev
         self.table = torch.empty(max(self.info["device_table_bytes"], 16), dtype=torch.uint8, device=d)
         zs.zs_plan_upload(self.plan, self.table, self.table.numel())
@@ -189,7 +191,7 @@ class DevicePlan:
 
     def snapshot(self):
         torch.cuda.synchronize()
-        N, S = self.N, self.op.S
+        N, S = self.op.group, self.op.S
         out = {}
         for k, b in self.bufs.items():
             a = b.u16() if b.t.dtype == torch.int16 else b.np()

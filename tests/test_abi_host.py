@@ -41,13 +41,17 @@ def _cpp_plan(numel, N, ds_id=None, **kw):
     return zs.zs_build_partition(cfg, numel, ds_id)
 
 
-def _compare(numel, N, ds_id=None, threshold=100_000, B=5_000_000, G=50_000_000, U=10**9):
+def _compare(numel, N, ds_id=None, threshold=100_000, B=5_000_000, G=50_000_000, U=10**9,
+             group=0):
     op = oplan.build_partition(numel, N, threshold=threshold, reduce_bucket_size=B,
-                               prefetch_bucket_size=G, sub_group_size=U, ds_id=ds_id)
+                               prefetch_bucket_size=G, sub_group_size=U, ds_id=ds_id,
+                               shard_group_size=group or None)
     cp = _cpp_plan(numel, N, ds_id, param_persistence_threshold=threshold,
-                   reduce_bucket_size=B, prefetch_bucket_size=G, sub_group_size=U)
+                   reduce_bucket_size=B, prefetch_bucket_size=G, sub_group_size=U,
+                   shard_group_size=group)
     info = zs.zs_plan_info(cp)
     assert info["n_params"] == len(numel)
+    assert info["n_ranks"] == N and info["shard_group_size"] == op.group
     assert info["shard_elems"] == op.S and info["shard_elems_logical"] == op.S_logical
     assert info["persist_elems"] == op.Pn_alloc and info["persist_elems_logical"] == op.Pn
     assert info["flat_elems"] == op.flat_elems and info["psi"] == op.psi
@@ -104,6 +108,19 @@ def test_cpp_plan_equals_oracle_workloads(name):
     _compare(w.numel, w.n_ranks, threshold=w.persistence_threshold)
 
 
+@pytest.mark.parametrize("N,group", [(8, 2), (16, 4), (12, 3), (64, 8), (6, 1)])
+def test_cpp_plan_equals_oracle_hsdp(N, group):
+    rng = np.random.default_rng(N * 7 + group)
+    numel = [int(x) for x in rng.integers(0, 4000, size=40)]
+    op, cp = _compare(numel, N, threshold=30, B=1500, G=6000, U=900, group=group)
+    _check_tiles(op, cp)
+
+
+def test_hsdp_group_must_divide_n():
+    with pytest.raises(zs.ZsError):
+        _cpp_plan([10], 8, shard_group_size=3)
+
+
 def test_cpp_plan_equals_oracle_many_small():
     w = workloads.many_small(2000)
     op, cp = _compare(w.numel, w.n_ranks, threshold=w.persistence_threshold)
@@ -129,7 +146,7 @@ def _check_tiles(op, cp):
     once, and each valid element maps to the bucket position and input
     position the oracle's definitions give."""
     t = zs.zs_plan_table(cp)
-    N, S = op.n_ranks, op.S
+    N, S = op.group, op.S
     cover = np.zeros(N * S, dtype=np.int32)
     pcover = np.zeros(op.Pn_alloc, dtype=np.int32)
     # expected source of each valid shard element: (bucket, src index, input index)

@@ -33,7 +33,8 @@ def _oracle_plan(w):
     return oplan.build_partition(w.numel, w.n_ranks, threshold=w.persistence_threshold,
                                  reduce_bucket_size=w.reduce_bucket_size,
                                  prefetch_bucket_size=w.prefetch_bucket_size,
-                                 sub_group_size=w.sub_group_size, ds_id=w.ds_id, dtype=w.dtype)
+                                 sub_group_size=w.sub_group_size, ds_id=w.ds_id, dtype=w.dtype,
+                                 shard_group_size=w.shard_group_size or None)
 
 
 def _grads(w, idx):
@@ -45,7 +46,7 @@ def _grads(w, idx):
 def _samples(op, rng, n_random=3000):
     """(rank, column) of random shard elements plus the first, last,
     padding and alignment columns of 40 random partitioned parameters."""
-    N, S = op.n_ranks, op.S
+    N, S = op.group, op.S            # shard rows: a group's owners
     rs = list(rng.integers(0, N, size=n_random))
     cs = list(rng.integers(0, S, size=n_random))
     part = [p for p in op.params if not p.persistent and p.ps > 0]
@@ -90,7 +91,7 @@ def _locate(op, w, dw, cols, ranks):
 
 
 @pytest.mark.parametrize("name", ["llama_layer", "many_small", "llama3_16_layers", "llama3_8b",
-                                  "llama3_8b_fp16"])
+                                  "llama3_8b_fp16", "llama3_8b_hsdp"])
 def test_fullsize_sampled(name):
     w = workloads.WORKLOADS[name]()
     op = _oracle_plan(w)
@@ -111,7 +112,7 @@ def test_fullsize_sampled(name):
         kind, win, pidx = _locate(op, w, dw, cols, ranks)
         data = kind == 0
         vals = _grads(w, pidx[:, data].ravel()).reshape(op.n_ranks, -1)
-        gs_ref = ostep.reduce_mean(vals, w.dtype)
+        gs_ref = ostep.reduce_mean_groups(vals, op.group, w.dtype)
         W = philox.weight_f32(w.seed, win[data].astype(np.uint64), w.weight_sigma)
         z = np.zeros_like(W)
         p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, coef,
@@ -152,7 +153,7 @@ def test_fullsize_sampled(name):
             pidx2 = torch.tensor([x[0] for x in ents], device=dw.dev)
             pv = _grads(w, np.array([x[2] for x in ents], dtype=np.uint64).T.ravel()
                         ).reshape(op.n_ranks, -1)
-            gP_ref = ostep.reduce_mean(pv, w.dtype)
+            gP_ref = ostep.reduce_mean_groups(pv, op.group, w.dtype)
             assert np.array_equal(dw.gP.index_select(0, pidx2).cpu().numpy().view(np.uint16), gP_ref)
             Wp = philox.weight_f32(w.seed, np.array([x[1] for x in ents], dtype=np.uint64),
                                    w.weight_sigma)
@@ -162,7 +163,7 @@ def test_fullsize_sampled(name):
             H.assert_f32_close(dw.pm.index_select(0, pidx2).cpu().numpy(), pp1, "p_master")
         # the norm is the norm of the reduced-gradient buffers
         tot = 0.0
-        for buf, n in ((dw.gs, op.n_ranks * op.S), (dw.gP, op.Pn_alloc)):
+        for buf, n in ((dw.gs, op.group * op.S), (dw.gP, op.Pn_alloc)):
             for ch in buf[:n].split(1 << 27):
                 x = ch.view(torch.float16 if w.dtype == "fp16" else torch.bfloat16).double()
                 tot += float((x * x).sum())

@@ -42,7 +42,8 @@ class ZsError(RuntimeError):
 class zs_config(C.Structure):
     _fields_ = [("n_ranks", C.c_int32), ("dtype", C.c_int32),
                 ("param_persistence_threshold", C.c_int64), ("reduce_bucket_size", C.c_int64),
-                ("prefetch_bucket_size", C.c_int64), ("sub_group_size", C.c_int64)]
+                ("prefetch_bucket_size", C.c_int64), ("sub_group_size", C.c_int64),
+                ("shard_group_size", C.c_int32), ("reserved", C.c_int32)]
 
 
 class zs_adam_hparams(C.Structure):
@@ -53,7 +54,8 @@ class zs_adam_hparams(C.Structure):
 
 class zs_plan_info_t(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("n_ranks", "n_params", "n_reduce_buckets",
-                                         "n_gather_buckets", "n_sub_groups", "dtype")] + \
+                                         "n_gather_buckets", "n_sub_groups", "dtype",
+                                         "shard_group_size", "reserved")] + \
                [(n, C.c_int64) for n in ("psi", "shard_elems", "shard_elems_logical",
                                          "persist_elems", "persist_elems_logical", "flat_elems",
                                          "padding_elems", "max_bucket_buf_elems",

@@ -143,7 +143,7 @@ zs_status zs_reduce_scatter(const zs_plan *P, int32_t bucket, const void *const 
     if (norm_scratch && !al(norm_scratch, 8))
         return zs_fail(ZS_EINVAL, "%s: norm_scratch not 8-byte aligned", fn);
     const ZsBucket &b = P->buckets[bucket];
-    return cuda_status(zsl_reduce_scatter(P->d_tiles, b.first_tile, b.n_tiles, rank_grads, N,
+    return cuda_status(zsl_reduce_scatter(P->d_tiles, b.first_tile, b.n_tiles, rank_grads, N, P->G,
                                           P->cfg.dtype,
                                           static_cast<uint16_t *>(grad_shards),
                                           static_cast<uint16_t *>(persist_grads), norm_scratch,
@@ -189,7 +189,7 @@ zs_status zs_adam_step(const zs_plan *P, int32_t sub_group, const zs_adam_hparam
         const ZsSubGroup &g = P->sub_groups[sub_group];
         s_lo = g.s_lo; s_hi = g.s_hi; p_lo = g.p_lo; p_hi = g.p_hi;
     }
-    return cuda_status(zsl_adam(P->cfg.n_ranks, P->cfg.dtype, P->S, s_lo, s_hi, p_lo, p_hi, c, d_clip_coef,
+    return cuda_status(zsl_adam(P->G, P->cfg.dtype, P->S, s_lo, s_hi, p_lo, p_hi, c, d_clip_coef,
                                 d_flags, *st, (cudaStream_t)stream), fn);
 }
 
@@ -215,7 +215,7 @@ zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *pa
     // ds_id order: every rank packs the same order ([ZeRO-3 chapter] §5.2, §7)
     std::sort(srt.begin(), srt.end(),
               [&](int32_t a, int32_t b) { return P->params[a].position < P->params[b].position; });
-    const int64_t N = P->cfg.n_ranks;
+    const int64_t N = P->G;   // a group's shard owners
     std::vector<int64_t> off((size_t)np, -1);
     int64_t total = 0;
     for (int32_t k : srt) {
@@ -314,7 +314,7 @@ zs_status zs_reduce_scatter_all(const zs_plan *P, const void *const *d_rank_grad
         return zs_fail(ZS_EINVAL, "%s: persist_grads NULL or not 16-byte aligned", fn);
     if ((r = check_scratch(P, norm_scratch, fn))) return r;
     return cuda_status(zsl_reduce_scatter_all(P->d_tiles, (int64_t)P->tiles.size(), d_rank_grads,
-                                              P->cfg.n_ranks, P->cfg.dtype,
+                                              P->cfg.n_ranks, P->G, P->cfg.dtype,
                                               static_cast<uint16_t *>(grad_shards),
                                               static_cast<uint16_t *>(persist_grads), norm_scratch,
                                               (cudaStream_t)stream), fn);

@@ -64,6 +64,7 @@ struct zs_plan {
     std::vector<ZsTile> tiles;
     int64_t S = 0, S_logical = 0, Pn_alloc = 0, Pn = 0, psi = 0, flat_elems = 0;
     int64_t padding = 0, max_buf = 0, max_gather = 0, n_level1 = 1;
+    int32_t G = 1;                     // shard owners per group (N unless HSDP)
     const ZsTile *d_tiles = nullptr;   // caller memory given to zs_plan_upload
 };
 

@@ -21,11 +21,11 @@ struct ZsScaleArgs {
 };
 
 cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                               const void *const *rank_ptrs, int N, int dtype, uint16_t *gs,
+                               const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
                                uint16_t *gP, double *partials, cudaStream_t s);
 
 cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
-                                   const void *const *d_table, int N, int dtype, uint16_t *gs,
+                                   const void *const *d_table, int N, int G, int dtype, uint16_t *gs,
                                    uint16_t *gP, double *partials, cudaStream_t s);
 
 cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,

@@ -28,7 +28,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t align8(int64_t x) { return (x + 7) / 8 * 8; }
 
 void emit_partitioned_tiles(zs_plan &P, const ZsParam &p, const ZsEntry &e, int32_t bucket) {
-    const int64_t N = P.cfg.n_ranks, ps = p.ps;
+    const int64_t N = P.G, ps = p.ps;   // shard owners
     if (ps == 0) return;
     // the bucket holding the last element also owns the padding numel..N*ps-1
     const int64_t hi = (e.e_hi == p.numel) ? N * ps : e.e_hi;
@@ -75,7 +75,9 @@ void emit_persistent_tiles(zs_plan &P, const ZsParam &p, const ZsEntry &e, int32
 
 zs_status build(zs_plan &P, int32_t n, const int64_t *numel, const int64_t *ds_id) {
     const zs_config &c = P.cfg;
-    const int64_t N = c.n_ranks;
+    // every layout is over the G shard owners of a replica group
+    P.G = c.shard_group_size > 0 ? c.shard_group_size : c.n_ranks;
+    const int64_t N = P.G;
     P.params.resize(n);
     for (int32_t i = 0; i < n; ++i) {
         ZsParam &p = P.params[i];
@@ -254,6 +256,8 @@ void zs_default_config(zs_config *cfg, int32_t n_ranks) {
     if (!cfg) return;
     cfg->n_ranks = n_ranks;
     cfg->dtype = ZS_DTYPE_BF16;
+    cfg->shard_group_size = 0;
+    cfg->reserved = 0;
     cfg->param_persistence_threshold = 100000;
     cfg->reduce_bucket_size = 5000000;
     cfg->prefetch_bucket_size = 50000000;
@@ -265,6 +269,11 @@ zs_status zs_build_partition(const zs_config *cfg, int32_t n_params, const int64
     if (!cfg || !out) return zs_fail(ZS_EINVAL, "zs_build_partition: NULL config or output");
     *out = nullptr;
     if (cfg->n_ranks < 1) return zs_fail(ZS_EINVAL, "zs_build_partition: n_ranks must be >= 1");
+    if (cfg->reserved != 0) return zs_fail(ZS_EINVAL, "zs_build_partition: reserved field must be 0");
+    if (cfg->shard_group_size < 0 ||
+        (cfg->shard_group_size > 0 && cfg->n_ranks % cfg->shard_group_size != 0))
+        return zs_fail(ZS_EINVAL, "zs_build_partition: shard_group_size %d must divide n_ranks %d",
+                       cfg->shard_group_size, cfg->n_ranks);
     if (cfg->dtype != ZS_DTYPE_BF16 && cfg->dtype != ZS_DTYPE_FP16)
         return zs_fail(ZS_EINVAL, "zs_build_partition: dtype must be ZS_DTYPE_BF16 or ZS_DTYPE_FP16");
     if (cfg->reduce_bucket_size < 1 || cfg->prefetch_bucket_size < 1 || cfg->sub_group_size < 1)
@@ -302,6 +311,7 @@ zs_status zs_plan_info(const zs_plan *P, zs_plan_info_t *o) {
     o->n_gather_buckets = (int32_t)P->gathers.size();
     o->n_sub_groups = (int32_t)P->sub_groups.size();
     o->dtype = P->cfg.dtype;
+    o->shard_group_size = P->G;
     o->psi = P->psi;
     o->shard_elems = P->S;
     o->shard_elems_logical = P->S_logical;

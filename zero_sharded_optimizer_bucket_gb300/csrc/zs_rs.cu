@@ -22,7 +22,7 @@ struct RankPtrs {
 template <bool FROM_TABLE, class T>
 __global__ void __launch_bounds__(THREADS, 5)
 rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
-          const uint16_t *const *__restrict__ table, int N, float fN,
+          const uint16_t *const *__restrict__ table, int N, int G, float fN,
           uint16_t *__restrict__ gs, uint16_t *__restrict__ gP, double *__restrict__ partials) {
     __shared__ const uint16_t *sp[ZS_MAX_RANKS];
     __shared__ double red[WARPS];
@@ -75,19 +75,37 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
         if (act) {
             const uint16_t *const *__restrict__ p = sp;
-            if (lo <= 0 && hi >= 8) {
+            if (G == N) {
+                if (lo <= 0 && hi >= 8) {
 #pragma unroll 8
-                for (int k = 0; k < N; ++k) {
-                    const uint4 v = ldg16(p[k] + 8 * c);
+                    for (int k = 0; k < N; ++k) {
+                        const uint4 v = ldg16(p[k] + 8 * c);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
+                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
+                    }
+                } else {
+#pragma unroll 4
+                    for (int k = 0; k < N; ++k) {
+                        const uint4 v = mask8(ldg16(p[k] + 8 * c), lo, hi);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
+                    }
                 }
             } else {
-#pragma unroll 4
-                for (int k = 0; k < N; ++k) {
-                    const uint4 v = mask8(ldg16(p[k] + 8 * c), lo, hi);
+                // HSDP: each replica group's G ranks in rank order, then the
+                // group sums in group order
+                for (int g0 = 0; g0 < N; g0 += G) {
+                    float in[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
+                    for (int i = 0; i < 8; ++i) in[i] = 0.0f;
+#pragma unroll 4
+                    for (int j = 0; j < G; ++j) {
+                        const uint4 v = mask8(ldg16(p[g0 + j] + 8 * c), lo, hi);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) in[i] = __fadd_rn(in[i], T::to_f32(lane16(v, i)));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], in[i]);
                 }
             }
         }
@@ -248,37 +266,37 @@ using namespace zsk;
 
 template <class T>
 static cudaError_t launch_rs(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                             const RankPtrs &p, const void *const *d_table, int N, uint16_t *gs,
+                             const RankPtrs &p, const void *const *d_table, int N, int G, uint16_t *gs,
                              uint16_t *gP, double *partials, cudaStream_t s) {
     if (d_table)
         rs_kernel<true, T><<<(unsigned)ntiles, THREADS, 0, s>>>(
-            d_tiles, tile0, p, reinterpret_cast<const uint16_t *const *>(d_table), N, (float)N, gs,
-            gP, partials);
+            d_tiles, tile0, p, reinterpret_cast<const uint16_t *const *>(d_table), N, G, (float)N,
+            gs, gP, partials);
     else
-        rs_kernel<false, T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, tile0, p, nullptr, N,
+        rs_kernel<false, T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, tile0, p, nullptr, N, G,
                                                                  (float)N, gs, gP, partials);
     return cudaGetLastError();
 }
 
 cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                               const void *const *rank_ptrs, int N, int dtype, uint16_t *gs,
+                               const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
                                uint16_t *gP, double *partials, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p;
     for (int k = 0; k < N; ++k) p.p[k] = static_cast<const uint16_t *>(rank_ptrs[k]);
     return dtype == ZS_DTYPE_FP16
-               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, nullptr, N, gs, gP, partials, s)
-               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, nullptr, N, gs, gP, partials, s);
+               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s);
 }
 
 cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
-                                   const void *const *d_table, int N, int dtype, uint16_t *gs,
+                                   const void *const *d_table, int N, int G, int dtype, uint16_t *gs,
                                    uint16_t *gP, double *partials, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p = {};
     return dtype == ZS_DTYPE_FP16
-               ? launch_rs<FP16T>(d_tiles, 0, ntiles, p, d_table, N, gs, gP, partials, s)
-               : launch_rs<BF16T>(d_tiles, 0, ntiles, p, d_table, N, gs, gP, partials, s);
+               ? launch_rs<FP16T>(d_tiles, 0, ntiles, p, d_table, N, G, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, 0, ntiles, p, d_table, N, G, gs, gP, partials, s);
 }
 
 cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,
