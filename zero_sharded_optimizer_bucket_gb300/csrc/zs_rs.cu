@@ -94,15 +94,27 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
             } else {
                 // HSDP: each replica group's G ranks in rank order, then the
                 // group sums in group order
+                const bool full = lo <= 0 && hi >= 8;
                 for (int g0 = 0; g0 < N; g0 += G) {
                     float in[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) in[i] = 0.0f;
-#pragma unroll 4
-                    for (int j = 0; j < G; ++j) {
-                        const uint4 v = mask8(ldg16(p[g0 + j] + 8 * c), lo, hi);
+                    if (full) {
+#pragma unroll 8
+                        for (int j = 0; j < G; ++j) {
+                            const uint4 v = ldg16(p[g0 + j] + 8 * c);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) in[i] = __fadd_rn(in[i], T::to_f32(lane16(v, i)));
+                            for (int i = 0; i < 8; ++i)
+                                in[i] = __fadd_rn(in[i], T::to_f32(lane16(v, i)));
+                        }
+                    } else {
+#pragma unroll 4
+                        for (int j = 0; j < G; ++j) {
+                            const uint4 v = mask8(ldg16(p[g0 + j] + 8 * c), lo, hi);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                in[i] = __fadd_rn(in[i], T::to_f32(lane16(v, i)));
+                        }
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], in[i]);
