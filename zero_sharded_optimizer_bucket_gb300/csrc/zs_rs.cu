@@ -19,7 +19,7 @@ struct RankPtrs {
     const uint16_t *p[ZS_MAX_RANKS];
 };
 
-template <bool FROM_TABLE, class T>
+template <bool FROM_TABLE, class T, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 5)
 rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
           const uint16_t *const *__restrict__ table, int N, int G, float fN,
@@ -75,7 +75,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
         if (act) {
             const uint16_t *const *__restrict__ p = sp;
-            if (G == N) {
+            if (!GROUPED) {
                 if (lo <= 0 && hi >= 8) {
 #pragma unroll 8
                     for (int k = 0; k < N; ++k) {
@@ -280,13 +280,15 @@ template <class T>
 static cudaError_t launch_rs(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
                              const RankPtrs &p, const void *const *d_table, int N, int G, uint16_t *gs,
                              uint16_t *gP, double *partials, cudaStream_t s) {
-    if (d_table)
-        rs_kernel<true, T><<<(unsigned)ntiles, THREADS, 0, s>>>(
-            d_tiles, tile0, p, reinterpret_cast<const uint16_t *const *>(d_table), N, G, (float)N,
-            gs, gP, partials);
-    else
-        rs_kernel<false, T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, tile0, p, nullptr, N, G,
-                                                                 (float)N, gs, gP, partials);
+    const auto *tbl = reinterpret_cast<const uint16_t *const *>(d_table);
+    const dim3 g((unsigned)ntiles), b(THREADS);
+    if (G == N) {
+        if (d_table) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
+        else rs_kernel<false, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, nullptr, N, G, (float)N, gs, gP, partials);
+    } else {
+        if (d_table) rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
+        else rs_kernel<false, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, nullptr, N, G, (float)N, gs, gP, partials);
+    }
     return cudaGetLastError();
 }
 
