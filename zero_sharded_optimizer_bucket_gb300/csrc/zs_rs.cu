@@ -93,31 +93,40 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
                 }
             } else {
                 // HSDP: each replica group's G ranks in rank order, then the
-                // group sums in group order
+                // group sums in group order.  Loads go in batches of 4 ranks
+                // whatever G is, so that short groups keep loads in flight;
+                // the group boundary is a warp-uniform counter.
                 const bool full = lo <= 0 && hi >= 8;
-                for (int g0 = 0; g0 < N; g0 += G) {
-                    float in[8];
+                float in[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) in[i] = 0.0f;
-                    if (full) {
-#pragma unroll 8
-                        for (int j = 0; j < G; ++j) {
-                            const uint4 v = ldg16(p[g0 + j] + 8 * c);
+                for (int i = 0; i < 8; ++i) in[i] = 0.0f;
+                int cnt = 0;
+                for (int k0 = 0; k0 < N; k0 += 4) {
+                    uint4 v[4];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                in[i] = __fadd_rn(in[i], T::to_f32(lane16(v, i)));
-                        }
-                    } else {
-#pragma unroll 4
-                        for (int j = 0; j < G; ++j) {
-                            const uint4 v = mask8(ldg16(p[g0 + j] + 8 * c), lo, hi);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                in[i] = __fadd_rn(in[i], T::to_f32(lane16(v, i)));
+                    for (int u = 0; u < 4; ++u) {
+                        v[u] = make_uint4(0, 0, 0, 0);
+                        if (k0 + u < N) {
+                            v[u] = ldg16(p[k0 + u] + 8 * c);
+                            if (!full) v[u] = mask8(v[u], lo, hi);
                         }
                     }
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], in[i]);
+                    for (int u = 0; u < 4; ++u) {
+                        if (k0 + u < N) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                in[i] = __fadd_rn(in[i], T::to_f32(lane16(v[u], i)));
+                            if (++cnt == G) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    acc[i] = __fadd_rn(acc[i], in[i]);
+                                    in[i] = 0.0f;
+                                }
+                                cnt = 0;
+                            }
+                        }
+                    }
                 }
             }
         }
