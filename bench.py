@@ -622,6 +622,101 @@ def run_reference(args):
     }), flush=True)
 
 
+def llama_modules(w):
+    """Modules of a Llama-shaped parameter list: the embedding, per layer an
+    attention module (q, k, v, o, input norm) and an MLP module (gate, up,
+    down, post-attention norm), then the final norm with the output head."""
+    idx = {n: i for i, n in enumerate(w.names)}
+    mods = [[idx["embed_tokens"]]] if "embed_tokens" in idx else []
+    layers = sorted({int(n.split(".")[1]) for n in w.names if n.startswith("layers.")})
+    for L in layers:
+        a = [f"layers.{L}.{x}" for x in ("q_proj", "k_proj", "v_proj", "o_proj", "input_layernorm")]
+        b = [f"layers.{L}.{x}" for x in ("gate_proj", "up_proj", "down_proj",
+                                          "post_attention_layernorm")]
+        mods.append([idx[n] for n in a])
+        mods.append([idx[n] for n in b])
+    tail = [idx[n] for n in ("norm", "lm_head") if n in idx]
+    if tail:
+        mods.append(tail)
+    return mods
+
+
+def run_gather_schedule(args):
+    """Forward + backward gathers of the workload's modules through the
+    gather scheduler, against a stand-in compute of ns_per_elem per element
+    of each module: compute alone, gathers alone, both with prefetch, both
+    without prefetch (prefetch_bucket_size 0)."""
+    import torch
+
+    import zero_sharded_optimizer_bucket_gb300 as zs
+    from synth import gpu as sg
+    dev = torch.device("cuda", 0)
+    w = load_workload(args.workload)
+    dw = DeviceWorkload(w, dev, pool_elems=1)
+    mods = llama_modules(w)
+    order = list(range(len(mods))) + list(reversed(range(len(mods))))
+    G = dw.info["shard_group_size"]
+    mod_elems = [sum(w.numel[p] for p in m) for m in mods]
+    largest = max(sum(G * zs.zs_param_info(dw.plan, p)["partition_size"] for p in set(m))
+                  for m in mods)
+    base = dict(prefetch_bucket_size=w.prefetch_bucket_size, max_live_parameters=1_000_000_000,
+                max_reuse_distance=1_000_000_000)
+    arena_elems = base["max_live_parameters"] + 2 * largest
+    arena = torch.empty(arena_elems, dtype=torch.int16, device=dev)
+    sink = torch.zeros(4, device=dev)
+    comp, gath = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # calibrate the stand-in compute: ns per FMA step on 152*4 CTAs
+    blocks = 152 * 4
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sg.busy(10000, blocks, sink, comp)
+    e0.record(comp)
+    sg.busy(200000, blocks, sink, comp)
+    e1.record(comp)
+    torch.cuda.synchronize(dev)
+    ns_per_iter = e0.elapsed_time(e1) * 1e6 / 200000
+    iters = [int(args.ns_per_elem * n / ns_per_iter) for n in mod_elems]
+
+    def run(mode, cfg=None, passes=3):
+        sched = zs.zs_sched_create(dw.plan, mods, dict(cfg, arena_elems=arena_elems),
+                                   arena) if cfg else None
+        times = []
+        for k in range(passes):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(comp)
+            for m in order:
+                if sched:
+                    zs.zs_sched_fetch(sched, m, dw.ps, comp, gath)
+                if mode != "gathers":
+                    sg.busy(iters[m], blocks, sink, comp)
+                if sched:
+                    zs.zs_sched_release(sched, m, comp)
+            if sched:
+                zs.zs_sched_end_pass(sched, comp)
+            comp.wait_stream(gath)
+            b.record(comp)
+            torch.cuda.synchronize(dev)
+            if k > 0:                   # pass 0 records the trace
+                times.append(a.elapsed_time(b))
+        st = zs.zs_sched_stats(sched) if sched else None
+        return sum(times) / len(times), st
+
+    t_comp, _ = run("compute")
+    t_gath, st_g = run("gathers", base)
+    t_over, st = run("both", base)
+    t_serial, _ = run("both", dict(base, prefetch_bucket_size=0))
+    gathered = 2 * sum(w.numel[p] for m in mods for p in m if not zs.zs_param_info(dw.plan, p)["persistent"])
+    res = {"mode": "gather_schedule", "workload": w.name, "modules": len(mods),
+           "passes": "forward + backward, " + str(len(order)) + " fetches",
+           "ns_per_elem_compute": args.ns_per_elem,
+           "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
+           "no_prefetch_ms": t_serial,
+           "hidden_fraction_of_gather": (t_comp + t_gath - t_over) / t_gath,
+           "gathers_only_gbs": 2 * 2 * gathered / (t_gath * 1e-3) / 1e9 if t_gath else None,
+           "sched_stats": st, "config": dict(base, arena_elems=arena_elems)}
+    print(json.dumps(res), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -633,12 +728,18 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--gather-schedule", action="store_true",
+                    help="measure the forward/backward gather scheduler instead of the step")
+    ap.add_argument("--ns-per-elem", type=float, default=1.0,
+                    help="stand-in compute per parameter element (gather-schedule mode)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "zs":
         print("bench.py: at least 3 warm-up steps are required", file=sys.stderr)
         return 2
     if args.impl == "reference":
         run_reference(args)
+    elif args.gather_schedule:
+        run_gather_schedule(args)
     else:
         run_gpu(args)
     return 0

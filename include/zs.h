@@ -436,6 +436,86 @@ zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_gr
                                const zs_loss_scaler *scaler, float *d_norm, float *d_clip_coef,
                                int32_t *d_flags, void *flat_out, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Gather scheduler — the forward / backward fetch and release of gathered
+ * parameters ([ZeRO-3 chapter] §5.1-5.3 PartitionedParameterCoordinator:
+ * trace, fetch_sub_module, release_sub_module; §7: an order change
+ * invalidates the trace).  A model is given as modules, each a list of
+ * parameter indices.  Each pass calls, per module in execution order,
+ * zs_sched_fetch (gathers what is missing, prefetches ahead along the
+ * recorded trace, makes the compute stream wait), then the caller's compute
+ * on the compute stream, then zs_sched_release.  zs_sched_end_pass releases
+ * everything (the optimizer step repartitions all parameters, §6.3).
+ * Rules:
+ * - the first pass records the module order; later passes prefetch from it;
+ *   a fetch that differs from the recorded order stops prefetching for the
+ *   pass and the next pass records again;
+ * - prefetch walks the trace's parameter uses after the current module,
+ *   skipping available / in-flight / persistent parameters, into one
+ *   coalesced gather while the elements added stay below
+ *   min(prefetch_bucket_size, max_live_parameters - live elements);
+ * - release keeps a parameter whose next use in the trace is within
+ *   max_reuse_distance elements of parameter uses;
+ * - gathers go to the caller's arena (bf16/fp16, arena_elems elements):
+ *   one contiguous block per gather, first fit, parameters laid out as
+ *   zs_all_gather_coalesced lays them; a gather reusing released space waits
+ *   on the compute stream's release event.
+ * Gathers are enqueued on the gather stream, which the compute stream waits
+ * on through CUDA events; neither call blocks the host. */
+typedef struct zs_sched zs_sched;   /* opaque, host memory + CUDA events */
+
+typedef struct {
+    int64_t prefetch_bucket_size;   /* elements, e.g. 5e7                     */
+    int64_t max_live_parameters;    /* elements gathered at once, e.g. 1e9    */
+    int64_t max_reuse_distance;     /* elements, e.g. 1e9                     */
+    int64_t arena_elems;            /* capacity of the arena                  */
+} zs_sched_config;
+
+typedef struct {
+    int64_t passes, gathers, params_gathered, elems_gathered, elems_prefetched;
+    int64_t fetch_misses;           /* parameters gathered by the fetch itself */
+    int64_t max_live_elems, max_arena_elems, invalidations;
+} zs_sched_stats_t;
+
+/* One record of the scheduler's log (for inspection and tests):
+ * kind 1 gather: op, module position, param, offset, aux = release waited (-1)
+ * kind 2 wait:   the compute of the module position waits for gather op
+ *                (op -1: nothing to wait for)
+ * kind 3 release: param released (-1: none) after the module position,
+ *                aux = release index */
+typedef struct {
+    int32_t kind, module_pos, op, param;
+    int64_t offset, aux;
+} zs_sched_event;
+
+/* Build a scheduler for the plan's parameters.  module_offsets[n_modules+1]
+ * and module_params (CSR) list each module's parameter indices.  d_arena is
+ * the device arena (16-byte aligned, arena_elems 2-byte elements), or NULL
+ * for a plan-only scheduler that makes no CUDA call (its log and stats are
+ * the same).  Errors: ZS_EINVAL (bad module list, parameter out of range,
+ * arena smaller than the largest module), ZS_ECUDA, ZS_ENOMEM. */
+zs_status zs_sched_create(const zs_plan *plan, int32_t n_modules, const int32_t *module_offsets,
+                          const int32_t *module_params, const zs_sched_config *cfg,
+                          void *d_arena, zs_sched **out);
+void zs_sched_destroy(zs_sched *sched);
+
+/* Fetch a module: param_shards is the plan's shard buffer [N][S].
+ * Errors: ZS_EINVAL (module out of range), ZS_ENOMEM (the module's missing
+ * parameters do not fit the arena), ZS_ECUDA. */
+zs_status zs_sched_fetch(zs_sched *sched, int32_t module, const void *param_shards,
+                         void *compute_stream, void *gather_stream);
+/* Release after the module's compute (enqueued on compute_stream). */
+zs_status zs_sched_release(zs_sched *sched, int32_t module, void *compute_stream);
+/* End of a pass: release everything; completes or resets the trace. */
+zs_status zs_sched_end_pass(zs_sched *sched, void *compute_stream);
+/* Arena offset of the view of a gathered parameter (valid between the fetch
+ * and the release of a module using it); -1 for a persistent parameter.
+ * Errors: ZS_EINVAL (index), ZS_ESTATE (not gathered now). */
+zs_status zs_sched_param_offset(const zs_sched *sched, int32_t param, int64_t *offset);
+zs_status zs_sched_stats(const zs_sched *sched, zs_sched_stats_t *out);
+/* Copy up to cap log records; *n receives the total count. */
+zs_status zs_sched_log(const zs_sched *sched, zs_sched_event *out, int64_t cap, int64_t *n);
+
 #ifdef __cplusplus
 }
 #endif

