@@ -459,7 +459,10 @@ zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_gr
  * - gathers go to the caller's arena (bf16/fp16, arena_elems elements):
  *   one contiguous block per gather, first fit, parameters laid out as
  *   zs_all_gather_coalesced lays them; a gather reusing released space waits
- *   on the compute stream's release event.
+ *   on the compute stream's release event.  Size the arena for the live
+ *   budget (max_live_parameters, padded to G*ps per parameter) plus what the
+ *   reuse distance keeps plus the largest module, with slack for first-fit
+ *   fragmentation; a fetch that does not fit fails with ZS_ENOMEM.
  * Gathers are enqueued on the gather stream, which the compute stream waits
  * on through CUDA events; neither call blocks the host. */
 typedef struct zs_sched zs_sched;   /* opaque, host memory + CUDA events */

@@ -33,8 +33,10 @@ def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch):
     expect = ostep.gather_model(d.op, d.ost.param_shards)
     mods = [[int(x) for x in rng.integers(0, 30, size=int(rng.integers(1, 5)))] for _ in range(14)]
     largest = max(sum(N * d.op.params[p].ps for p in set(m)) for m in mods)
+    # the arena holds the live budget (plus padding) and the largest module,
+    # with arena_factor of slack for fragmentation
     cfg = dict(prefetch_bucket_size=prefetch, max_live_parameters=60000,
-               max_reuse_distance=20000, arena_elems=int(largest * arena_factor) + 64)
+               max_reuse_distance=20000, arena_elems=int((60000 + 2 * largest) * arena_factor))
     arena = torch.full((cfg["arena_elems"],), -1, dtype=torch.int16, device=d.dev)
     sched = zs.zs_sched_create(d.plan, mods, cfg, arena)
     oracle = osched.Scheduler(d.op, mods, osched.SchedConfig(**cfg))
