@@ -701,16 +701,20 @@ def run_gather_schedule(args):
         st = zs.zs_sched_stats(sched) if sched else None
         return sum(times) / len(times), st
 
+    clocks = ClockSampler(_gpu_uuid(torch, dev))
+    clocks.start()
     t_comp, _ = run("compute")
     t_gath, st_g = run("gathers", base)
     t_over, st = run("both", base)
     t_serial, _ = run("both", dict(base, prefetch_bucket_size=0))
+    t_over2, _ = run("both", base)
+    ck = clocks.stop()
     gathered = 2 * sum(w.numel[p] for m in mods for p in m if not zs.zs_param_info(dw.plan, p)["persistent"])
     res = {"mode": "gather_schedule", "workload": w.name, "modules": len(mods),
            "passes": "forward + backward, " + str(len(order)) + " fetches",
            "ns_per_elem_compute": args.ns_per_elem,
            "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
-           "no_prefetch_ms": t_serial,
+           "prefetch_overlapped_repeat_ms": t_over2, "no_prefetch_ms": t_serial, "clocks": ck,
            "hidden_fraction_of_gather": (t_comp + t_gath - t_over) / t_gath,
            "gathers_only_gbs": 2 * 2 * gathered / (t_gath * 1e-3) / 1e9 if t_gath else None,
            "sched_stats": st, "config": dict(base, arena_elems=arena_elems)}
@@ -730,8 +734,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--gather-schedule", action="store_true",
                     help="measure the forward/backward gather scheduler instead of the step")
-    ap.add_argument("--ns-per-elem", type=float, default=1.0,
-                    help="stand-in compute per parameter element (gather-schedule mode)")
+    ap.add_argument("--ns-per-elem", type=float, default=0.002,
+                    help="stand-in compute per parameter element and pass (gather-schedule "
+                         "mode); 0.002 ns is 6 flops x ~570 tokens at 1.7 PFLOP/s")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "zs":
         print("bench.py: at least 3 warm-up steps are required", file=sys.stderr)
