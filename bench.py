@@ -708,6 +708,9 @@ def run_gather_schedule(args):
     t_over, st = run("both", base)
     t_serial, _ = run("both", dict(base, prefetch_bucket_size=0))
     t_over2, _ = run("both", base)
+    sweep = {}
+    for pb in (200_000_000, 1_000_000_000):
+        sweep[str(pb)] = run("both", dict(base, prefetch_bucket_size=pb))[0]
     ck = clocks.stop()
     gathered = 2 * sum(w.numel[p] for m in mods for p in m if not zs.zs_param_info(dw.plan, p)["persistent"])
     res = {"mode": "gather_schedule", "workload": w.name, "modules": len(mods),
@@ -715,6 +718,7 @@ def run_gather_schedule(args):
            "ns_per_elem_compute": args.ns_per_elem,
            "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
            "prefetch_overlapped_repeat_ms": t_over2, "no_prefetch_ms": t_serial, "clocks": ck,
+           "prefetch_bucket_sweep_ms": sweep,
            "hidden_fraction_of_gather": (t_comp + t_gath - t_over) / t_gath,
            "gathers_only_gbs": 2 * 2 * gathered / (t_gath * 1e-3) / 1e9 if t_gath else None,
            "sched_stats": st, "config": dict(base, arena_elems=arena_elems)}

@@ -457,7 +457,8 @@ zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_gr
  * - release keeps a parameter whose next use in the trace is within
  *   max_reuse_distance elements of parameter uses;
  * - gathers go to the caller's arena (bf16/fp16, arena_elems elements):
- *   one contiguous block per gather, first fit, parameters laid out as
+ *   one contiguous block per gather, in the fitting free segment released
+ *   longest ago (never used first, then lowest offset), laid out as
  *   zs_all_gather_coalesced lays them; a gather reusing released space waits
  *   on the compute stream's release event.  Size the arena for the live
  *   budget (max_live_parameters, padded to G*ps per parameter) plus what the

@@ -34,11 +34,12 @@ pages only name the mechanism):
   (max_live_parameters, §5.3).  Persistent parameters are never gathered.
 * Arena.  A gather takes one contiguous block of G*ps elements per
   parameter, laid out as zs_all_gather_coalesced lays them (running sums in
-  ds_id order), found first-fit over the free segments of the arena (lowest
-  offset first); a release frees the parameter's own segment, adjacent free
-  segments merge.  A gather whose block reuses space freed by releases waits
-  for the latest of those releases.  A current fetch that does not fit is an
-  error.
+  ds_id order), at the start of the free segment that fits and was released
+  longest ago (never-used space first, then the lowest offset), so that a
+  prefetch seldom waits for a recent compute; a release frees the
+  parameter's own segment, adjacent free segments merge (keeping the later
+  release).  A gather whose block reuses released space waits for the latest
+  release of that segment.  A current fetch that does not fit is an error.
 
 The log is a list of tuples:
   ("gather", op, module_pos, [(param, offset)...], wait_release)  wait_release
@@ -101,21 +102,23 @@ class Scheduler:
         return [(k, p) for k, m in enumerate(self.trace) for p in self.modules[m]]
 
     def _alloc(self, params):
-        """First-fit block for the params in ds_id order; returns
-        (offsets, wait_release) or None."""
+        """One block for the params in ds_id order, at the start of the
+        fitting free segment released longest ago (never used first, then
+        the lowest offset); returns (offsets, wait_release) or None."""
         srt = sorted(params, key=lambda i: self.plan.params[i].ds_id)
         total = sum(self._size(p) for p in srt)
-        for k, (off, size, rel) in enumerate(self.free):
-            if size >= total:
-                waits = rel
-                rest = (off + total, size - total, rel)
-                self.free[k:k + 1] = [rest] if rest[1] > 0 else []
-                offs, run = {}, off
-                for p in srt:
-                    offs[p] = run
-                    run += self._size(p)
-                return offs, waits
-        return None
+        fits = [(rel, off, k) for k, (off, size, rel) in enumerate(self.free) if size >= total]
+        if not fits:
+            return None
+        _, _, k = min(fits)
+        off, size, rel = self.free[k]
+        rest = (off + total, size - total, rel)
+        self.free[k:k + 1] = [rest] if rest[1] > 0 else []
+        offs, run = {}, off
+        for p in srt:
+            offs[p] = run
+            run += self._size(p)
+        return offs, rel
 
     def _free(self, p, rel):
         off, size = self.offset.pop(p), self._size(p)

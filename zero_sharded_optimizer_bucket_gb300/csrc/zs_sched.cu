@@ -61,15 +61,23 @@ void sort_ds(const zs_sched *s, std::vector<int32_t> &v) {
     });
 }
 
-// First fit of one block for the parameters (ds_id order); on success the
-// free list is updated and offsets / the release to wait for are returned.
+// One block for the parameters (ds_id order) in the fitting free segment
+// released longest ago; on success the free list is updated and offsets /
+// the release to wait for are returned.
 bool alloc(zs_sched *s, std::vector<int32_t> params, std::vector<int64_t> &offs, int64_t &waits) {
     sort_ds(s, params);
     int64_t total = 0;
     for (int32_t p : params) total += psize(s, p);
+    // the fitting segment released longest ago (never used first), then the
+    // lowest offset: a prefetch then seldom waits for a recent compute
+    int64_t best = -1;
     for (size_t k = 0; k < s->free_.size(); ++k) {
-        const Seg g = s->free_[k];
+        const Seg &g = s->free_[k];
         if (g.size < total) continue;
+        if (best < 0 || g.rel < s->free_[best].rel) best = (int64_t)k;
+    }
+    for (int64_t k = best; k >= 0; k = -1) {
+        const Seg g = s->free_[k];
         waits = g.rel;
         if (g.size > total)
             s->free_[k] = Seg{g.off + total, g.size - total, g.rel};
