@@ -665,15 +665,32 @@ def run_gather_schedule(args):
     arena = torch.empty(arena_elems, dtype=torch.int16, device=dev)
     sink = torch.zeros(4, device=dev)
     comp, gath = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    # calibrate the stand-in compute: ns per FMA step on 152*4 CTAs
-    blocks = 152 * 4
+    # stand-in compute: one warp per SM running a dependent FMA chain takes
+    # time without taking the SMs' issue slots or memory bandwidth (as
+    # tensor-core compute leaves them); calibrate its ns per step
+    blocks, threads = 152, 32
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sg.busy(10000, blocks, sink, comp)
+    sg.busy(10000, blocks, sink, comp, threads)
     e0.record(comp)
-    sg.busy(200000, blocks, sink, comp)
+    sg.busy(200000, blocks, sink, comp, threads)
     e1.record(comp)
     torch.cuda.synchronize(dev)
     ns_per_iter = e0.elapsed_time(e1) * 1e6 / 200000
+    # concurrency probe: the same compute beside one large gather on the other stream
+    probe_params = [p for p in range(len(w.numel))
+                    if not zs.zs_param_info(dw.plan, p)["persistent"]][:8]
+    pr_elems = sum(G * zs.zs_param_info(dw.plan, p)["partition_size"] for p in probe_params)
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(comp)
+    sg.busy(200000, blocks, sink, comp, threads)
+    e1.record(comp)
+    e2.record(gath)
+    zs.zs_all_gather_coalesced(dw.plan, probe_params, dw.ps, arena, pr_elems, gath)
+    e3.record(gath)
+    torch.cuda.synchronize(dev)
+    probe = {"compute_ms_alone": ns_per_iter * 200000 / 1e6, "compute_ms_beside_gather":
+             e0.elapsed_time(e1), "gather_ms_beside_compute": e2.elapsed_time(e3)}
     iters = [int(args.ns_per_elem * n / ns_per_iter) for n in mod_elems]
 
     def run(mode, cfg=None, passes=3):
@@ -688,7 +705,7 @@ def run_gather_schedule(args):
                 if sched:
                     zs.zs_sched_fetch(sched, m, dw.ps, comp, gath)
                 if mode != "gathers":
-                    sg.busy(iters[m], blocks, sink, comp)
+                    sg.busy(iters[m], blocks, sink, comp, threads)
                 if sched:
                     zs.zs_sched_release(sched, m, comp)
             if sched:
@@ -718,7 +735,7 @@ def run_gather_schedule(args):
            "ns_per_elem_compute": args.ns_per_elem,
            "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
            "prefetch_overlapped_repeat_ms": t_over2, "no_prefetch_ms": t_serial, "clocks": ck,
-           "prefetch_bucket_sweep_ms": sweep,
+           "prefetch_bucket_sweep_ms": sweep, "concurrency_probe": probe,
            "hidden_fraction_of_gather": (t_comp + t_gath - t_over) / t_gath,
            "gathers_only_gbs": 2 * 2 * gathered / (t_gath * 1e-3) / 1e9 if t_gath else None,
            "sched_stats": st, "config": dict(base, arena_elems=arena_elems)}

@@ -120,10 +120,13 @@ int zsg_fill_grad_fp16(void *out, int64_t start, int64_t count, uint64_t seed, u
     return (int)cudaGetLastError();
 }
 
-// Busy compute of `iters` FMA steps per thread on `blocks` CTAs of 256.
-int zsg_busy(int64_t iters, int blocks, float *sink, void *stream) {
-    if (iters <= 0 || blocks <= 0) return 0;
-    busy_kernel<<<blocks, THREADS, 0, (cudaStream_t)stream>>>(iters, sink);
+// Busy compute of `iters` FMA steps per thread on `blocks` CTAs of
+// `threads` threads (a multiple of 32, at most 256).  With one warp per SM
+// the dependent chain takes time while leaving the SM's issue slots and the
+// memory system to other streams, the way tensor-core compute does.
+int zsg_busy(int64_t iters, int blocks, int threads, float *sink, void *stream) {
+    if (iters <= 0 || blocks <= 0 || threads <= 0 || threads > THREADS || threads % 32) return 0;
+    busy_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(iters, sink);
     return (int)cudaGetLastError();
 }
 

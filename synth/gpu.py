@@ -24,7 +24,7 @@ def _load():
         lib.zsg_fill_grad_fp16.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_uint64,
                                            C.c_uint32, C.c_int, C.c_uint32, C.c_int, C.c_void_p]
         lib.zsg_busy.restype = C.c_int
-        lib.zsg_busy.argtypes = [C.c_int64, C.c_int, C.c_void_p, C.c_void_p]
+        lib.zsg_busy.argtypes = [C.c_int64, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         lib.zsg_fill_normal_f32.restype = C.c_int
         lib.zsg_fill_normal_f32.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_uint64,
                                             C.c_uint32, C.c_uint32, C.c_float, C.c_void_p]
@@ -68,8 +68,9 @@ def fill_grad_fp16(t, start: int, seed: int, log2_scale: int, outlier_frac: floa
         raise RuntimeError(f"zsg_fill_grad_fp16: CUDA error {err}")
 
 
-def busy(iters: int, blocks: int, sink, stream=None) -> None:
-    """Stand-in compute: `blocks` CTAs of 256 threads, `iters` FMAs each."""
-    err = _load().zsg_busy(int(iters), int(blocks), sink.data_ptr(), _stream(stream))
+def busy(iters: int, blocks: int, sink, stream=None, threads: int = 256) -> None:
+    """Stand-in compute: `blocks` CTAs of `threads` threads, `iters` FMAs each."""
+    err = _load().zsg_busy(int(iters), int(blocks), int(threads), sink.data_ptr(),
+                           _stream(stream))
     if err:
         raise RuntimeError(f"zsg_busy: CUDA error {err}")

@@ -47,7 +47,7 @@ def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch):
         for m in order:
             zs.zs_sched_fetch(sched, m, d.bufs["param_shards"].ptr(), comp, gath)
             oracle.fetch(m)
-            sgpu.busy(20000, 152, sink, comp)            # slow compute before reading
+            sgpu.busy(20000, 152, sink, comp, 256)       # slow compute before reading
             views = {}
             for p in set(mods[m]):
                 off = zs.zs_sched_param_offset(sched, p)
