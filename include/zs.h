@@ -451,9 +451,10 @@ zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_gr
  *   a fetch that differs from the recorded order stops prefetching for the
  *   pass and the next pass records again;
  * - prefetch walks the trace's parameter uses after the current module,
- *   skipping available / in-flight / persistent parameters, into one
- *   coalesced gather while the elements added stay below
- *   min(prefetch_bucket_size, max_live_parameters - live elements);
+ *   skipping available / in-flight / persistent parameters, while the
+ *   elements added stay below min(prefetch_bucket_size,
+ *   max_live_parameters - live elements), one coalesced gather per module
+ *   reached (a compute then waits only for its own module's gather);
  * - release keeps a parameter whose next use in the trace is within
  *   max_reuse_distance elements of parameter uses;
  * - gathers go to the caller's arena (bf16/fp16, arena_elems elements):

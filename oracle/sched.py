@@ -18,9 +18,11 @@ pages only name the mechanism):
   (3) with a COMPLETE trace, prefetch: walk the parameter queue (every
   (position, parameter) use of the trace after the current position, in
   order), skipping parameters already available / in flight and persistent
-  ones, adding the others to one coalesced gather while the elements added
-  so far are below min(prefetch_bucket_size, max_live_parameters - live
-  elements); a parameter that would not fit the arena ends the walk.  The
+  ones, gathering the others while the elements added so far are below
+  min(prefetch_bucket_size, max_live_parameters - live elements), one
+  coalesced gather per module of the trace reached (so a compute waits only
+  for its own module's gather); a parameter that would not fit the arena
+  ends the walk.  The
   walk resumes where it stopped at the next fetch (it never goes back
   before the next module's entries).
 * Release (§5.3 release_sub_module, __params_to_release).  After the
@@ -175,15 +177,19 @@ class Scheduler:
         start = sum(len(self.modules[self.trace[k]]) for k in range(pos + 1))
         self.queue_pos = max(self.queue_pos, start)
         cap = min(self.cfg.prefetch_bucket_size, self.cfg.max_live_parameters - self.live)
-        group, added = [], 0
+        group, gpos, added = [], -1, 0
         while self.queue_pos < len(queue) and added < cap:
-            _, p = queue[self.queue_pos]
+            k, p = queue[self.queue_pos]
             if not self._gatherable(p) or p in self.status or p in group:
                 self.queue_pos += 1
                 continue
+            if group and k != gpos:          # one coalesced gather per module reached
+                self._gather(group, pos, False)
+                group = []
             if self._alloc_probe(group + [p]) is None:
                 break
             group.append(p)
+            gpos = k
             added += self.plan.params[p].numel
             self.queue_pos += 1
         self._gather(group, pos, False)

@@ -180,11 +180,20 @@ bool probe(zs_sched *s, const std::vector<int32_t> &params) {
     return ok;
 }
 
+// Walk the trace's parameter uses after the current module within the
+// budget; one coalesced gather per module reached, so that a compute waits
+// only for the gather of its own parameters.
 zs_status prefetch(zs_sched *s, int64_t pos, const void *shards, void *gstream) {
     s->queue_pos = std::max(s->queue_pos, s->queue_start[pos + 1]);
     const int64_t cap = std::min(s->cfg.prefetch_bucket_size, s->cfg.max_live_parameters - s->live);
     std::vector<int32_t> group;
-    int64_t added = 0;
+    int64_t gpos = -1, added = 0;
+    zs_status r;
+    // trace position of queue entry i
+    auto position_of = [&](int64_t i) {
+        return (int64_t)(std::upper_bound(s->queue_start.begin(), s->queue_start.end() - 1, i) -
+                         s->queue_start.begin()) - 1;
+    };
     while (s->queue_pos < (int64_t)s->queue.size() && added < cap) {
         const int32_t p = s->queue[s->queue_pos];
         if (!gatherable(s, p) || s->live_flag[p] ||
@@ -192,11 +201,17 @@ zs_status prefetch(zs_sched *s, int64_t pos, const void *shards, void *gstream) 
             ++s->queue_pos;
             continue;
         }
+        const int64_t k = position_of(s->queue_pos);
+        if (!group.empty() && k != gpos) {
+            if ((r = gather(s, group, pos, shards, gstream, true))) return r;
+            group.clear();
+        }
         group.push_back(p);
         if (!probe(s, group)) {
             group.pop_back();
             break;
         }
+        gpos = k;
         added += numel(s, p);
         ++s->queue_pos;
     }
