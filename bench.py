@@ -721,6 +721,16 @@ def run_gather_schedule(args):
     clocks = ClockSampler(_gpu_uuid(torch, dev))
     clocks.start()
     t_comp, _ = run("compute")
+    # gather grid caps: the whole GPU, then one and two CTAs per SM (room
+    # left for the compute stream's blocks, as a collective's channels leave)
+    by_ctas = {}
+    for c in (0, 152, 304):
+        cfg = dict(base, gather_ctas=c)
+        by_ctas[str(c)] = {"gathers_only_ms": run("gathers", cfg)[0],
+                           "prefetch_overlapped_ms": run("both", cfg)[0],
+                           "no_prefetch_ms": run("both", dict(cfg, prefetch_bucket_size=0))[0]}
+    best = min(by_ctas, key=lambda c: by_ctas[c]["prefetch_overlapped_ms"])
+    base = dict(base, gather_ctas=int(best))
     t_gath, st_g = run("gathers", base)
     t_over, st = run("both", base)
     t_serial, _ = run("both", dict(base, prefetch_bucket_size=0))
@@ -736,6 +746,7 @@ def run_gather_schedule(args):
            "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
            "prefetch_overlapped_repeat_ms": t_over2, "no_prefetch_ms": t_serial, "clocks": ck,
            "prefetch_bucket_sweep_ms": sweep, "concurrency_probe": probe,
+           "by_gather_ctas": by_ctas,
            "hidden_fraction_of_gather": (t_comp + t_gath - t_over) / t_gath,
            "gathers_only_gbs": 2 * 2 * gathered / (t_gath * 1e-3) / 1e9 if t_gath else None,
            "sched_stats": st, "config": dict(base, arena_elems=arena_elems)}

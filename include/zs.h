@@ -458,8 +458,9 @@ zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_gr
  * - release keeps a parameter whose next use in the trace is within
  *   max_reuse_distance elements of parameter uses;
  * - gathers go to the caller's arena (bf16/fp16, arena_elems elements):
- *   one contiguous block per gather, in the fitting free segment released
- *   longest ago (never used first, then lowest offset), laid out as
+ *   one contiguous block per gather, placed where the latest release of
+ *   the free space it covers is oldest (never used first, then lowest
+ *   offset), laid out as
  *   zs_all_gather_coalesced lays them; a gather reusing released space waits
  *   on the compute stream's release event.  Size the arena for the live
  *   budget (max_live_parameters, padded to G*ps per parameter) plus what the
@@ -474,6 +475,11 @@ typedef struct {
     int64_t max_live_parameters;    /* elements gathered at once, e.g. 1e9    */
     int64_t max_reuse_distance;     /* elements, e.g. 1e9                     */
     int64_t arena_elems;            /* capacity of the arena                  */
+    int64_t gather_ctas;            /* CTAs per gather launch, 0..2^20: 0 lets
+                                       a gather take the whole GPU; a cap
+                                       (e.g. 152, one per SM) leaves room for
+                                       the compute stream's kernels, as a
+                                       collective's few channels would      */
 } zs_sched_config;
 
 typedef struct {

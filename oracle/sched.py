@@ -36,12 +36,12 @@ pages only name the mechanism):
   (max_live_parameters, §5.3).  Persistent parameters are never gathered.
 * Arena.  A gather takes one contiguous block of G*ps elements per
   parameter, laid out as zs_all_gather_coalesced lays them (running sums in
-  ds_id order), at the start of the free segment that fits and was released
-  longest ago (never-used space first, then the lowest offset), so that a
-  prefetch seldom waits for a recent compute; a release frees the
-  parameter's own segment, adjacent free segments merge (keeping the later
-  release).  A gather whose block reuses released space waits for the latest
-  release of that segment.  A current fetch that does not fit is an error.
+  ds_id order).  Free space is kept as segments tagged with the release that
+  freed them (neighbours merge only when freed by the same release); a
+  block may span adjacent segments and then waits for the latest of their
+  releases; the placement with the oldest such release (never-used space
+  first), then the lowest offset, is taken, so that a prefetch seldom waits
+  for a recent compute.  A current fetch that does not fit is an error.
 
 The log is a list of tuples:
   ("gather", op, module_pos, [(param, offset)...], wait_release)  wait_release
@@ -104,33 +104,49 @@ class Scheduler:
         return [(k, p) for k, m in enumerate(self.trace) for p in self.modules[m]]
 
     def _alloc(self, params):
-        """One block for the params in ds_id order, at the start of the
-        fitting free segment released longest ago (never used first, then
-        the lowest offset); returns (offsets, wait_release) or None."""
+        """One block for the params in ds_id order.  Free space is a sorted
+        list of segments, each with the release that freed it; a block may
+        span adjacent segments and waits for the latest release among them.
+        The placement chosen has the oldest such release (never-used space
+        first), then the lowest offset.  Returns (offsets, wait_release) or
+        None."""
         srt = sorted(params, key=lambda i: self.plan.params[i].ds_id)
         total = sum(self._size(p) for p in srt)
-        fits = [(rel, off, k) for k, (off, size, rel) in enumerate(self.free) if size >= total]
-        if not fits:
+        best = None
+        n = len(self.free)
+        for i in range(n):
+            acc, wait = 0, -1
+            for j in range(i, n):
+                off_j, size_j, rel_j = self.free[j]
+                if j > i and self.free[j - 1][0] + self.free[j - 1][1] != off_j:
+                    break
+                acc += size_j
+                wait = max(wait, rel_j)
+                if acc >= total:
+                    cand = (wait, self.free[i][0], i, j, acc)
+                    if best is None or cand[:2] < best[:2]:
+                        best = cand
+                    break
+        if best is None:
             return None
-        _, _, k = min(fits)
-        off, size, rel = self.free[k]
-        rest = (off + total, size - total, rel)
-        self.free[k:k + 1] = [rest] if rest[1] > 0 else []
+        wait, off, i, j, acc = best
+        rest = acc - total
+        rel_j = self.free[j][2]
+        self.free[i:j + 1] = [(off + total, rest, rel_j)] if rest > 0 else []
         offs, run = {}, off
         for p in srt:
             offs[p] = run
             run += self._size(p)
-        return offs, rel
+        return offs, wait
 
     def _free(self, p, rel):
         off, size = self.offset.pop(p), self._size(p)
-        segs = self.free + [(off, size, rel)]
-        segs.sort()
+        segs = sorted(self.free + [(off, size, rel)])
         merged = []
-        for s in segs:
-            if merged and merged[-1][0] + merged[-1][1] == s[0]:
+        for s in segs:            # merge neighbours freed by the same release
+            if merged and merged[-1][0] + merged[-1][1] == s[0] and merged[-1][2] == s[2]:
                 a = merged[-1]
-                merged[-1] = (a[0], a[1] + s[1], max(a[2], s[2]))
+                merged[-1] = (a[0], a[1] + s[1], a[2])
             else:
                 merged.append(s)
         self.free = merged

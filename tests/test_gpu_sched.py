@@ -23,9 +23,11 @@ from tests.test_sched_host import _oracle_records  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("seed,N,arena_factor,prefetch", [(1, 4, 2.0, 30000), (2, 8, 1.3, 5000),
-                                                          (3, 3, 4.0, 100000), (4, 16, 1.1, 0)])
-def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch):
+@pytest.mark.parametrize("seed,N,arena_factor,prefetch,ctas",
+                         [(1, 4, 2.0, 30000, 0), (2, 8, 1.3, 5000, 1), (3, 3, 4.0, 100000, 3),
+                          (4, 16, 1.1, 0, 0), (5, 5, 1.5, 20000, 152)])
+def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas):
+    """ctas caps the gather grid (grid-stride loops cover the rest)."""
     rng = np.random.default_rng(seed)
     numel = [int(x) for x in rng.integers(1, 20000, size=30)]
     d = H.DevicePlan(numel, N, threshold=200, seed=seed)
@@ -38,7 +40,7 @@ def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch):
     cfg = dict(prefetch_bucket_size=prefetch, max_live_parameters=60000,
                max_reuse_distance=20000, arena_elems=int((60000 + 2 * largest) * arena_factor))
     arena = torch.full((cfg["arena_elems"],), -1, dtype=torch.int16, device=d.dev)
-    sched = zs.zs_sched_create(d.plan, mods, cfg, arena)
+    sched = zs.zs_sched_create(d.plan, mods, dict(cfg, gather_ctas=ctas), arena)
     oracle = osched.Scheduler(d.op, mods, osched.SchedConfig(**cfg))
     comp, gath = torch.cuda.Stream(), torch.cuda.Stream()
     sink = torch.zeros(4, device=d.dev)

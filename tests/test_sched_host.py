@@ -103,7 +103,6 @@ def test_invariants_on_a_transformer_like_model():
     numel.append(5000)
     mods.append([len(numel) - 1, 0])                  # tied output projection
     plan_o = oplan.build_partition(numel, N, threshold=100)
-    plan_c = zs.zs_build_partition(zs.zs_default_config(N), numel) if False else None
     cfg_c = zs.zs_default_config(N)
     cfg_c.param_persistence_threshold = 100
     plan_c = zs.zs_build_partition(cfg_c, numel)
@@ -130,3 +129,62 @@ def test_invariants_on_a_transformer_like_model():
         elif e[0] == 3 and e[3] >= 0:
             live.discard(e[3])
     assert not live
+
+
+def _replay_arena(log, size, arena_elems):
+    """Replays a log on an element-wise model of the arena: no gather lands
+    on space a live parameter holds, and each gather waits for exactly the
+    latest release that freed any element of its block (-1: never used)."""
+    owner = np.full(arena_elems, -1, dtype=np.int64)      # live parameter per element
+    freed = np.full(arena_elems, -1, dtype=np.int64)      # release that last freed it
+    where = {}
+    blocks = {}
+    for kind, pos, op, p, off, aux in log:
+        if kind == 1:
+            lo, hi = off, off + size(p)
+            assert hi <= arena_elems
+            assert (owner[lo:hi] == -1).all(), ("gather onto live space", op, p)
+            owner[lo:hi] = p
+            where[p] = (lo, hi)
+            b = blocks.setdefault(op, [aux, -1])
+            b[1] = max(b[1], int(freed[lo:hi].max()))
+        elif kind == 3 and p >= 0:
+            lo, hi = where.pop(p)
+            owner[lo:hi] = -1
+            freed[lo:hi] = aux
+    for op, (waits, need) in blocks.items():
+        assert waits == need, (op, waits, need)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_gathers_wait_for_exactly_the_releases_they_reuse(seed):
+    rng = np.random.default_rng(100 + seed)
+    N = int(rng.integers(2, 9))
+    numel, mods = _model(rng, 40, 16)
+    plan_o = oplan.build_partition(numel, N, threshold=int(rng.integers(0, 500)))
+    cfg_c = zs.zs_default_config(N)
+    cfg_c.param_persistence_threshold = plan_o.threshold
+    plan_c = zs.zs_build_partition(cfg_c, numel)
+    largest = max([sum(N * plan_o.params[p].ps for p in set(m)) for m in mods] + [1])
+    cfg = dict(prefetch_bucket_size=int(rng.integers(0, 20000)), max_live_parameters=30000,
+               max_reuse_distance=int(rng.integers(0, 20000)), arena_elems=3 * largest + 40000)
+    fwd = list(range(len(mods)))
+    order = fwd + list(reversed(fwd))
+    o, c, failed = _run_both(plan_o, plan_c, mods, cfg, [order] * 4)
+    assert not failed
+    log = zs.zs_sched_log(c)
+    assert log == _oracle_records(o.log)
+    _replay_arena(log, lambda p: N * plan_o.params[p].ps, cfg["arena_elems"])
+
+
+def test_gather_cta_cap_is_checked():
+    numel = [5000, 7000]
+    cfg_c = zs.zs_default_config(2)
+    plan_c = zs.zs_build_partition(cfg_c, numel)
+    base = dict(prefetch_bucket_size=0, max_live_parameters=100000, max_reuse_distance=0,
+                arena_elems=20000)
+    for bad in (-1, (1 << 20) + 1):
+        with pytest.raises(zs.ZsError) as ei:
+            zs.zs_sched_create(plan_c, [[0], [1]], dict(base, gather_ctas=bad))
+        assert ei.value.status == zs.ZS_EINVAL
+    assert zs.zs_sched_create(plan_c, [[0], [1]], dict(base, gather_ctas=152)).handle

@@ -99,7 +99,8 @@ class zs_shard_state(C.Structure):
 
 class zs_sched_config(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("prefetch_bucket_size", "max_live_parameters",
-                                         "max_reuse_distance", "arena_elems")]
+                                         "max_reuse_distance", "arena_elems",
+                                         "gather_ctas")]
 
 
 class zs_sched_stats_t(C.Structure):

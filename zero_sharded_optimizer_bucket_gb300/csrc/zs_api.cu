@@ -193,10 +193,11 @@ zs_status zs_adam_step(const zs_plan *P, int32_t sub_group, const zs_adam_hparam
                                 d_flags, *st, (cudaStream_t)stream), fn);
 }
 
-zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *params,
-                                  const void *param_shards, void *flat_out,
-                                  int64_t flat_capacity, int64_t *view_offsets, void *stream) {
-    const char *fn = "zs_all_gather_coalesced";
+}  // extern "C"
+
+zs_status zs_gather_impl(const zs_plan *P, int32_t n, const int32_t *params,
+                         const void *param_shards, void *flat_out, int64_t flat_capacity,
+                         int64_t *view_offsets, void *stream, int max_ctas, const char *fn) {
     zs_status r = need_table(P, fn);
     if (r) return r;
     if (n < 0 || (n > 0 && (!params || !view_offsets)))
@@ -240,7 +241,8 @@ zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *pa
     auto flush = [&]() -> zs_status {
         if (a.n == 0) return ZS_OK;
         const cudaError_t e = zsl_gather(a, static_cast<const uint16_t *>(param_shards),
-                                         static_cast<uint16_t *>(flat_out), (cudaStream_t)stream);
+                                         static_cast<uint16_t *>(flat_out), (cudaStream_t)stream,
+                                         max_ctas);
         a.n = 0;
         return cuda_status(e, fn);
     };
@@ -259,6 +261,15 @@ zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *pa
     for (int32_t i = 0; i < n; ++i) view_offsets[i] = off[params[i]];
     zs_clear_error();
     return ZS_OK;
+}
+
+extern "C" {
+
+zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *params,
+                                  const void *param_shards, void *flat_out,
+                                  int64_t flat_capacity, int64_t *view_offsets, void *stream) {
+    return zs_gather_impl(P, n, params, param_shards, flat_out, flat_capacity, view_offsets,
+                          stream, 0, "zs_all_gather_coalesced");
 }
 
 zs_status zs_unscale_and_clip(const zs_plan *P, const void *grad_shards, const void *persist_grads,

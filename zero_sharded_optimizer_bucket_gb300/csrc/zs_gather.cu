@@ -72,12 +72,13 @@ gather_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t *__r
 using namespace zsk;
 
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
-                       cudaStream_t s) {
+                       cudaStream_t s, int max_ctas) {
     if (a.n <= 0 || a.out_hi <= a.out_lo) return cudaSuccess;
     const int a0 = (int)((reinterpret_cast<uintptr_t>(flat_out) >> 1) & 7);
     const int64_t groups = ((a0 + a.out_hi - 1) >> 3) - ((a0 + a.out_lo) >> 3) + 1;
     int64_t blocks = (groups + THREADS - 1) / THREADS;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    const int64_t cap = max_ctas > 0 ? max_ctas : 152 * 8;
+    if (blocks > cap) blocks = cap;
     gather_kernel<<<(unsigned)blocks, THREADS, 0, s>>>(a, shards, flat_out, a0);
     return cudaGetLastError();
 }

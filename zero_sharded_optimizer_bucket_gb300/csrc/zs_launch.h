@@ -60,5 +60,6 @@ struct ZsGatherArgs {
     int64_t out_lo, out_hi;
 };
 
+// max_ctas caps the grid (0: up to 8 CTAs per SM)
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
-                       cudaStream_t s);
+                       cudaStream_t s, int max_ctas);

@@ -61,47 +61,56 @@ void sort_ds(const zs_sched *s, std::vector<int32_t> &v) {
     });
 }
 
-// One block for the parameters (ds_id order) in the fitting free segment
-// released longest ago; on success the free list is updated and offsets /
-// the release to wait for are returned.
+// One block for the parameters (ds_id order).  Free space is a sorted list
+// of segments tagged with the release that freed them; a block may span
+// adjacent segments and waits for the latest of their releases.  The
+// placement with the oldest such release (never used first), then the
+// lowest offset, is taken.  On success the free list is updated and the
+// offsets / the release to wait for are returned.
 bool alloc(zs_sched *s, std::vector<int32_t> params, std::vector<int64_t> &offs, int64_t &waits) {
     sort_ds(s, params);
     int64_t total = 0;
     for (int32_t p : params) total += psize(s, p);
-    // the fitting segment released longest ago (never used first), then the
-    // lowest offset: a prefetch then seldom waits for a recent compute
-    int64_t best = -1;
-    for (size_t k = 0; k < s->free_.size(); ++k) {
-        const Seg &g = s->free_[k];
-        if (g.size < total) continue;
-        if (best < 0 || g.rel < s->free_[best].rel) best = (int64_t)k;
-    }
-    for (int64_t k = best; k >= 0; k = -1) {
-        const Seg g = s->free_[k];
-        waits = g.rel;
-        if (g.size > total)
-            s->free_[k] = Seg{g.off + total, g.size - total, g.rel};
-        else
-            s->free_.erase(s->free_.begin() + (int64_t)k);
-        offs.clear();
-        int64_t run = g.off;
-        for (int32_t p : params) {
-            offs.push_back(run);
-            run += psize(s, p);
+    const int64_t n = (int64_t)s->free_.size();
+    int64_t bi = -1, bj = -1, bwait = 0, boff = 0, bacc = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t acc = 0, wait = -1;
+        for (int64_t j = i; j < n; ++j) {
+            const Seg &g = s->free_[j];
+            if (j > i && s->free_[j - 1].off + s->free_[j - 1].size != g.off) break;
+            acc += g.size;
+            wait = std::max(wait, g.rel);
+            if (acc >= total) {
+                const int64_t off = s->free_[i].off;
+                if (bi < 0 || wait < bwait || (wait == bwait && off < boff)) {
+                    bi = i, bj = j, bwait = wait, boff = off, bacc = acc;
+                }
+                break;
+            }
         }
-        return true;
     }
-    return false;
+    if (bi < 0) return false;
+    const int64_t rest = bacc - total, rel_j = s->free_[bj].rel;
+    s->free_.erase(s->free_.begin() + bi, s->free_.begin() + bj + 1);
+    if (rest > 0) s->free_.insert(s->free_.begin() + bi, Seg{boff + total, rest, rel_j});
+    waits = bwait;
+    offs.clear();
+    int64_t run = boff;
+    for (int32_t p : params) {
+        offs.push_back(run);
+        run += psize(s, p);
+    }
+    return true;
 }
 
 void free_seg(zs_sched *s, int32_t p, int64_t rel) {
     s->free_.push_back(Seg{s->offset[p], psize(s, p), rel});
     std::sort(s->free_.begin(), s->free_.end(), [](const Seg &a, const Seg &b) { return a.off < b.off; });
     std::vector<Seg> merged;
-    for (const Seg &g : s->free_) {
-        if (!merged.empty() && merged.back().off + merged.back().size == g.off) {
+    for (const Seg &g : s->free_) {  // merge neighbours freed by the same release
+        if (!merged.empty() && merged.back().off + merged.back().size == g.off &&
+            merged.back().rel == g.rel) {
             merged.back().size += g.size;
-            merged.back().rel = std::max(merged.back().rel, g.rel);
         } else {
             merged.push_back(g);
         }
@@ -159,8 +168,8 @@ zs_status gather(zs_sched *s, std::vector<int32_t> params, int64_t pos, const vo
         if (e != cudaSuccess) return cuda_err(e, "zs_sched: cudaStreamWaitEvent");
     }
     std::vector<int64_t> views(params.size());
-    r = zs_all_gather_coalesced(s->P, (int32_t)params.size(), params.data(), shards,
-                                s->arena + offs[0], block, views.data(), gstream);
+    r = zs_gather_impl(s->P, (int32_t)params.size(), params.data(), shards, s->arena + offs[0],
+                       block, views.data(), gstream, (int)s->cfg.gather_ctas, "zs_sched_fetch");
     if (r) return r;
     for (size_t i = 0; i < params.size(); ++i)
         if (views[i] != offs[i] - offs[0])
@@ -267,7 +276,7 @@ zs_status zs_sched_create(const zs_plan *P, int32_t n_modules, const int32_t *mo
         return zs_fail(ZS_EINVAL, "%s: bad arguments", fn);
     *out = nullptr;
     if (cfg->prefetch_bucket_size < 0 || cfg->max_live_parameters < 0 || cfg->max_reuse_distance < 0 ||
-        cfg->arena_elems < 0)
+        cfg->arena_elems < 0 || cfg->gather_ctas < 0 || cfg->gather_ctas > (1 << 20))
         return zs_fail(ZS_EINVAL, "%s: negative size in the configuration", fn);
     if (d_arena && (reinterpret_cast<uintptr_t>(d_arena) & 15))
         return zs_fail(ZS_EINVAL, "%s: arena not 16-byte aligned", fn);
