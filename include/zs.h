@@ -384,6 +384,17 @@ zs_status zs_all_gather_coalesced(const zs_plan *plan, int32_t n, const int32_t 
                                   const void *param_shards, void *flat_out,
                                   int64_t flat_capacity, int64_t *view_offsets, void *stream);
 
+/* Bounded waits that gave up, counted on the current device since the last
+ * reset.  A gather whose runs are all 16-byte aligned (flat_out 16-byte
+ * aligned, every partition_size a multiple of 8 and at least 1024) moves
+ * its bytes with TMA bulk copies through shared memory, one mbarrier wait
+ * per chunk; a wait that does not complete within a bound (about a second)
+ * is abandoned, the gather's output is then incomplete, and this counter
+ * goes up.  Synchronous (reads device memory).  reset != 0 sets it back to
+ * 0.  Has no counterpart in the pages: it is this library's report of its
+ * own bounded waits.  Errors: ZS_EINVAL (NULL count), ZS_ECUDA. */
+zs_status zs_device_wait_timeouts(int32_t *count, int32_t reset);
+
 /* A2 over every bucket in one launch — the first pass of zs_shard_step.
  * Same result as zs_reduce_scatter on each bucket in turn.  d_rank_grads
  * as in zs_shard_step; norm_scratch (>= norm_scratch_elems doubles) receives

@@ -21,6 +21,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import bench  # noqa: E402
+import zero_sharded_optimizer_bucket_gb300 as zs  # noqa: E402
 from oracle import plan as oplan  # noqa: E402
 from oracle import step as ostep  # noqa: E402
 from synth import philox, workloads  # noqa: E402
@@ -139,6 +140,17 @@ def test_fullsize_sampled(name):
             fsrc.append(s)
         fl = dw.flat.index_select(0, torch.tensor(fpos, device=dw.dev)).cpu().numpy()
         assert np.array_equal(fl.view(np.uint16), got["ps"].view(np.uint16)[fsrc])
+        # the same positions after zs_all_gather_coalesced of every gather
+        # bucket into a cleared flat buffer (the Llama plans take the
+        # bulk-copy path: all partition sizes are multiples of 8)
+        dw.flat.zero_()
+        for g in op.gather_buckets:
+            zs.zs_all_gather_coalesced(dw.plan, g.params, dw.ps, dw.flat[g.flat_off:],
+                                       g.flat_elems)
+        torch.cuda.synchronize()
+        fl = dw.flat.index_select(0, torch.tensor(fpos, device=dw.dev)).cpu().numpy()
+        assert np.array_equal(fl.view(np.uint16), got["ps"].view(np.uint16)[fsrc])
+        assert zs.zs_device_wait_timeouts() == 0
         # persistent parameters: sampled elements
         pers = [p for p in op.params if p.persistent and p.numel > 0]
         if pers:

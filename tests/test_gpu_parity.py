@@ -41,6 +41,11 @@ CASES = {
     "numel_lt_n": dict(numel=[1, 2, 3, 5, 0, 9, 17], N=16, threshold=0),
     "n1": dict(numel=[100, 7, 4099, 1], N=1, threshold=5, B=2048),
     "many_small_64": dict(numel=workloads.many_small(60).numel, N=64, threshold=100_000),
+    # partition sizes multiples of 8 and >= 1024: gathers into a 16-byte
+    # aligned buffer take the bulk-copy path, many 32 KB chunks long; the
+    # 70001-element parameter sends any request holding it to the other path
+    "aligned_bulk": dict(numel=[65536, 131136, 8192, 192000, 500, 1048576, 70001], N=8,
+                         threshold=1000, B=300_000),
 }
 
 
@@ -186,6 +191,7 @@ def test_all_gather_coalesced(case):
     with pytest.raises(zs.ZsError):
         zs.zs_all_gather_coalesced(d.plan, [0, 0], d.bufs["param_shards"].ptr(), d.flat.ptr(),
                                    d.op.flat_elems)
+    assert zs.zs_device_wait_timeouts() == 0
 
 
 def test_fused_equals_unfused(case):

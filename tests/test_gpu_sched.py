@@ -23,13 +23,21 @@ from tests.test_sched_host import _oracle_records  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("seed,N,arena_factor,prefetch,ctas",
-                         [(1, 4, 2.0, 30000, 0), (2, 8, 1.3, 5000, 1), (3, 3, 4.0, 100000, 3),
-                          (4, 16, 1.1, 0, 0), (5, 5, 1.5, 20000, 152)])
-def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas):
-    """ctas caps the gather grid (grid-stride loops cover the rest)."""
+@pytest.mark.parametrize("seed,N,arena_factor,prefetch,ctas,aligned",
+                         [(1, 4, 2.0, 30000, 0, False), (2, 8, 1.3, 5000, 1, False),
+                          (3, 3, 4.0, 100000, 3, False), (4, 16, 1.1, 0, 0, False),
+                          (5, 5, 1.5, 20000, 152, False), (6, 4, 1.5, 30000, 0, True),
+                          (7, 2, 1.3, 60000, 2, True)])
+def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas, aligned):
+    """ctas caps the gather grid (strided loops cover the rest).  aligned:
+    partition sizes are multiples of 8 and >= 1024, so every block of the
+    arena starts on a 16-byte boundary and the gathers take the bulk-copy
+    path."""
     rng = np.random.default_rng(seed)
-    numel = [int(x) for x in rng.integers(1, 20000, size=30)]
+    if aligned:
+        numel = [8 * N * int(x) for x in rng.integers(128, 2500 // N + 130, size=30)]
+    else:
+        numel = [int(x) for x in rng.integers(1, 20000, size=30)]
     d = H.DevicePlan(numel, N, threshold=200, seed=seed)
     d.init_weights()
     expect = ostep.gather_model(d.op, d.ost.param_shards)
@@ -69,6 +77,7 @@ def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas):
         zs.zs_sched_end_pass(sched, comp)
         oracle.end_pass()
     torch.cuda.synchronize()
+    assert zs.zs_device_wait_timeouts() == 0
     assert zs.zs_sched_log(sched) == _oracle_records(oracle.log)
     st = zs.zs_sched_stats(sched)
     if prefetch:

@@ -148,6 +148,7 @@ _sig("zs_grad_norm", _i32, [_P, _P, _P, _P, _i32, _f32, _P, _P, _P, _P])
 _sig("zs_adam_step", _i32, [_P, _i32, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                             C.POINTER(zs_shard_state), _P])
 _sig("zs_all_gather_coalesced", _i32, [_P, _i32, C.POINTER(_i32), _P, _P, _i64, C.POINTER(_i64), _P])
+_sig("zs_device_wait_timeouts", _i32, [C.POINTER(_i32), _i32])
 _sig("zs_reduce_scatter_all", _i32, [_P, _P, _P, _P, _P, _P])
 _sig("zs_adam_gather", _i32, [_P, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                               C.POINTER(zs_shard_state), _P, _P])
@@ -383,6 +384,13 @@ def zs_all_gather_coalesced(plan, params, param_shards, flat_out, flat_capacity:
                                         int(flat_capacity), views, _stream(stream)),
            "zs_all_gather_coalesced")
     return [views[i] for i in range(n)]
+
+
+def zs_device_wait_timeouts(reset: bool = False) -> int:
+    """Bounded device waits that gave up on the current device (synchronous)."""
+    c = _i32()
+    _check(_lib.zs_device_wait_timeouts(C.byref(c), int(bool(reset))), "zs_device_wait_timeouts")
+    return c.value
 
 
 def zs_shard_step(plan, d_rank_grads, state: zs_shard_state, norm_scratch, hp, step: int,

@@ -265,6 +265,16 @@ zs_status zs_gather_impl(const zs_plan *P, int32_t n, const int32_t *params,
 
 extern "C" {
 
+zs_status zs_device_wait_timeouts(int32_t *count, int32_t reset) {
+    if (!count) return zs_fail(ZS_EINVAL, "zs_device_wait_timeouts: NULL count");
+    int c = 0;
+    const cudaError_t e = zsl_bulk_wait_timeouts(&c, reset != 0);
+    if (e != cudaSuccess) return cuda_status(e, "zs_device_wait_timeouts");
+    *count = c;
+    zs_clear_error();
+    return ZS_OK;
+}
+
 zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *params,
                                   const void *param_shards, void *flat_out,
                                   int64_t flat_capacity, int64_t *view_offsets, void *stream) {

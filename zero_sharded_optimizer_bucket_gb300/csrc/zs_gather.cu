@@ -2,11 +2,15 @@
 // gather group ([ZeRO-3 chapter] §5.2: shards sorted by ds_id, one flat
 // buffer, per-parameter views).
 //
-// Output-centric: a thread owns 8 output slots aligned to 16 bytes in the
-// output's address space.  When the 8 slots come from one rank's shard of
-// one parameter they are one contiguous run of shard space: one 16-byte
-// load (two and a lane shift when the phases differ) and one 16-byte store.
-// Slots that straddle a shard boundary are assembled one by one.
+// Two paths.  When every run (rank r's shard of one parameter, landing at
+// out_off + r*ps) is 16-byte aligned at both ends in both buffers, TMA bulk
+// copies move the bytes (gather_bulk_kernel below).  Otherwise the SM path:
+// output-centric, a thread owns a group of 8 output slots aligned to 16
+// bytes in the output's address space.  When the 8 slots come from one
+// rank's shard of one parameter they are one contiguous run of shard space:
+// one 16-byte load (two and a lane shift when the phases differ) and one
+// 16-byte store.  Slots that straddle a shard boundary are assembled one by
+// one.
 #include "zs_device.cuh"
 #include "zs_launch.h"
 
@@ -67,18 +71,224 @@ gather_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t *__r
     }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy path.  When every run of the launch (rank r's shard of one
+// parameter, ps elements, landing at out_off + r*ps) starts and ends on a
+// 16-byte boundary in both buffers, the gather is a list of aligned memcpy
+// pieces.  One thread per CTA drives the TMA engine: it loads a chunk of
+// the output (BULK_CHUNK bytes, one or more pieces) from shard space into a
+// shared-memory stage with cp.async.bulk, waits on the stage's mbarrier,
+// and writes the chunk back to flat_out with one bulk store.  BULK_STAGES
+// chunks are in flight per CTA, so a CTA per SM keeps HBM busy while the
+// SMs' warps stay free for other kernels.
+#ifndef ZS_BULK_STAGES
+#define ZS_BULK_STAGES 3
+#endif
+#ifndef ZS_BULK_CHUNK
+#define ZS_BULK_CHUNK 32768
+#endif
+constexpr int BULK_STAGES = ZS_BULK_STAGES;
+constexpr int BULK_CHUNK = ZS_BULK_CHUNK;              // bytes per chunk (multiple of 16)
+constexpr int64_t BULK_CHUNK_ELEMS = BULK_CHUNK / 2;
+constexpr int BULK_SMEM = BULK_STAGES * BULK_CHUNK;
+constexpr int BULK_SMEM_ALLOC = BULK_SMEM + 8 * BULK_STAGES;   // + mbarriers
+constexpr long long BULK_WAIT_LIMIT = 1ll << 22;       // try_wait calls per wait
+
+__device__ int g_bulk_wait_timeouts;                    // waits that gave up
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (long long i = 0; i < BULK_WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// Issues the loads of chunk c (output elements [f, f_end)) into stage buffer
+// dst, completing on mbarrier bar; returns the chunk's bytes.
+__device__ uint32_t bulk_load_chunk(const ZsGatherArgs &a, const uint16_t *shards, int64_t c,
+                                    uint32_t dst, uint32_t bar) {
+    int64_t f = a.out_lo + c * BULK_CHUNK_ELEMS;
+    const int64_t f_end = min(f + BULK_CHUNK_ELEMS, a.out_hi);
+    const uint32_t bytes = (uint32_t)(2 * (f_end - f));
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :
+                 : "r"(bar), "r"(bytes)
+                 : "memory");
+    int lo = 0, hi = a.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.e[mid].out_off <= f) lo = mid; else hi = mid - 1;
+    }
+    int idx = lo;
+    int64_t r = (f - a.e[idx].out_off) / a.e[idx].ps;
+    int64_t j = (f - a.e[idx].out_off) - r * a.e[idx].ps;
+    uint32_t at = dst;
+    while (f < f_end) {
+        const int64_t len = min(f_end - f, a.e[idx].ps - j);
+        const uint16_t *src = shards + r * a.S + a.e[idx].shard_off + j;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+            "[%3];"
+            :
+            : "r"(at), "l"(src), "r"((uint32_t)(2 * len)), "r"(bar)
+            : "memory");
+        at += (uint32_t)(2 * len);
+        f += len;
+        j += len;
+        if (j == a.e[idx].ps) {
+            j = 0;
+            if (++r == a.N) {
+                r = 0;
+                ++idx;
+            }
+        }
+    }
+    return bytes;
+}
+
+__global__ void __launch_bounds__(32)
+gather_bulk_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t *__restrict__ out) {
+    // dynamic shared memory only: BULK_STAGES chunk buffers, then the
+    // stages' mbarriers
+    extern __shared__ __align__(128) uint8_t stage[];
+    if (threadIdx.x != 0) return;
+    const uint32_t base = smem_u32(stage);
+    if (base & 15) {                     // bulk copies need 16-byte aligned buffers
+        atomicAdd(&g_bulk_wait_timeouts, 1);
+        return;
+    }
+    // shared-window address of stage s's mbarrier (computed as an integer:
+    // the barriers lie past the chunk buffers in the dynamic allocation)
+    auto bar = [base](int64_t s) { return base + (uint32_t)(BULK_SMEM + 8 * s); };
+    const int64_t n_chunks = (a.out_hi - a.out_lo + BULK_CHUNK_ELEMS - 1) / BULK_CHUNK_ELEMS;
+    if ((int64_t)blockIdx.x >= n_chunks) return;
+    const int64_t mine = (n_chunks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    for (int s = 0; s < BULK_STAGES; ++s)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" : : "r"(bar(s)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" : : : "memory");
+    asm volatile("fence.proxy.async.shared::cta;" : : : "memory");
+    uint32_t bytes[BULK_STAGES];
+    const int64_t pre = mine < BULK_STAGES ? mine : BULK_STAGES;
+    for (int64_t k = 0; k < pre; ++k)
+        bytes[k] = bulk_load_chunk(a, shards, blockIdx.x + k * gridDim.x,
+                                   base + (uint32_t)(k * BULK_CHUNK), bar(k));
+    int64_t issued = pre;
+    bool ok = true;
+    for (int64_t k = 0; k < mine; ++k) {
+        const int s = (int)(k % BULK_STAGES);
+        if (!mbar_wait(bar(s), (uint32_t)((k / BULK_STAGES) & 1))) {
+            ok = false;
+            break;
+        }
+        const int64_t c = blockIdx.x + k * gridDim.x;
+        uint16_t *dst = out + a.out_lo + c * BULK_CHUNK_ELEMS;
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                     :
+                     : "l"(dst), "r"(base + (uint32_t)(s * BULK_CHUNK)), "r"(bytes[s])
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" : : : "memory");
+        if (issued < mine) {
+            // the stage is free again once the store has read it
+            asm volatile("cp.async.bulk.wait_group.read 0;" : : : "memory");
+            bytes[s] = bulk_load_chunk(a, shards, blockIdx.x + issued * gridDim.x,
+                                       base + (uint32_t)(s * BULK_CHUNK), bar(s));
+            ++issued;
+        }
+    }
+    if (!ok) {
+        // a wait gave up: count it and let the loads already issued land
+        // (each wait again bounded) before the CTA's shared memory goes away
+        atomicAdd(&g_bulk_wait_timeouts, 1);
+        for (int64_t k = 0; k < issued; ++k) {
+            const int s = (int)(k % BULK_STAGES);
+            if (k + BULK_STAGES < issued) continue;
+            mbar_wait(bar(s), (uint32_t)((k / BULK_STAGES) & 1));
+        }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" : : : "memory");
+}
+
 }  // namespace zsk
 
 using namespace zsk;
 
+namespace {
+
+// The bulk path needs every piece 16-byte aligned at both ends, and pieces
+// long enough to be worth a TMA request each.
+constexpr int64_t BULK_MIN_PS = 1024;
+
+bool bulk_ok(const ZsGatherArgs &a, const uint16_t *shards, const uint16_t *flat_out) {
+    if ((reinterpret_cast<uintptr_t>(flat_out) & 15) || (reinterpret_cast<uintptr_t>(shards) & 15))
+        return false;
+    if (a.S % 8 || a.out_lo % 8) return false;
+    int64_t next = a.out_lo;
+    for (int i = 0; i < a.n; ++i) {
+        const ZsGatherEntry &e = a.e[i];
+        if (e.ps < BULK_MIN_PS || e.ps % 8 || e.shard_off % 8 || e.out_off != next) return false;
+        next += (int64_t)a.N * e.ps;
+    }
+    return next == a.out_hi;
+}
+
+}  // namespace
+
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
                        cudaStream_t s, int max_ctas) {
     if (a.n <= 0 || a.out_hi <= a.out_lo) return cudaSuccess;
+    if (bulk_ok(a, shards, flat_out)) {
+        // per device: its SM count, and the kernel's shared-memory opt-in
+        // per device: the kernel's shared-memory opt-in, and the default
+        // grid of 8 CTAs per SM: CTAs queue behind the resident ones, which
+        // measured faster than one wave of resident CTAs
+        static int wave_of[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        int wave = wave_of[dev];
+        if (wave <= 0) {
+            int sms = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gather_bulk_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         BULK_SMEM_ALLOC);
+            if (e != cudaSuccess) return e;
+            wave = wave_of[dev] = 8 * (sms > 0 ? sms : 152);
+        }
+        const int64_t chunks = (a.out_hi - a.out_lo + BULK_CHUNK_ELEMS - 1) / BULK_CHUNK_ELEMS;
+        const int64_t cap = max_ctas > 0 ? max_ctas : wave;
+        const int64_t blocks = chunks < cap ? chunks : cap;
+        gather_bulk_kernel<<<(unsigned)blocks, 32, BULK_SMEM_ALLOC, s>>>(a, shards, flat_out);
+        return cudaGetLastError();
+    }
     const int a0 = (int)((reinterpret_cast<uintptr_t>(flat_out) >> 1) & 7);
     const int64_t groups = ((a0 + a.out_hi - 1) >> 3) - ((a0 + a.out_lo) >> 3) + 1;
     int64_t blocks = (groups + THREADS - 1) / THREADS;
-    const int64_t cap = max_ctas > 0 ? max_ctas : 152 * 8;
+    const int64_t cap = max_ctas > 0 ? max_ctas : 152 * 8;   // 8 CTAs of 256 fill an SM
     if (blocks > cap) blocks = cap;
     gather_kernel<<<(unsigned)blocks, THREADS, 0, s>>>(a, shards, flat_out, a0);
     return cudaGetLastError();
+}
+
+cudaError_t zsl_bulk_wait_timeouts(int *count, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_bulk_wait_timeouts, sizeof(int));
+    if (e == cudaSuccess && reset) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_bulk_wait_timeouts, &zero, sizeof(int));
+    }
+    return e;
 }

@@ -60,6 +60,8 @@ struct ZsGatherArgs {
     int64_t out_lo, out_hi;
 };
 
-// max_ctas caps the grid (0: up to 8 CTAs per SM)
+// max_ctas caps the grid (0: one wave of resident CTAs)
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
                        cudaStream_t s, int max_ctas);
+// Number of bounded waits of the bulk gather that gave up (synchronous).
+cudaError_t zsl_bulk_wait_timeouts(int *count, bool reset);
