@@ -276,7 +276,8 @@ def peaks():
 
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, when
-    it was taken on the kernel sources as they are now (else None)."""
+    it was taken on the kernel's device sources (the entry's "sources") as
+    they are now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -284,16 +285,22 @@ def ncu_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     ent = d.get(kernel)
-    if not ent or ent.get("sources_sha256") != sources_digest():
+    if not ent or not ent.get("sources"):
+        return None
+    try:
+        if ent.get("sources_sha256") != sources_digest(ent["sources"]):
+            return None
+    except OSError:
         return None
     return ent.get("dram_bytes_per_launch")
 
 
-def sources_digest():
+def sources_digest(files):
+    """sha256 over the named files of the package's csrc/, in sorted order."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "zero_sharded_optimizer_bucket_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()
@@ -693,7 +700,10 @@ def run_gather_schedule(args):
              e0.elapsed_time(e1), "gather_ms_beside_compute": e2.elapsed_time(e3)}
     iters = [int(args.ns_per_elem * n / ns_per_iter) for n in mod_elems]
 
-    def run(mode, cfg=None, passes=3):
+    def run(mode, cfg=None, passes=3, paced=False):
+        """paced: the host waits for each module's compute before the next
+        fetch (a loop that reads a value back every module), so only
+        gathers issued ahead by prefetch can overlap a compute."""
         sched = zs.zs_sched_create(dw.plan, mods, dict(cfg, arena_elems=arena_elems),
                                    arena) if cfg else None
         times = []
@@ -708,6 +718,8 @@ def run_gather_schedule(args):
                     sg.busy(iters[m], blocks, sink, comp, threads)
                 if sched:
                     zs.zs_sched_release(sched, m, comp)
+                if paced:
+                    comp.synchronize()
             if sched:
                 zs.zs_sched_end_pass(sched, comp)
             comp.wait_stream(gath)
@@ -738,6 +750,10 @@ def run_gather_schedule(args):
     sweep = {}
     for pb in (200_000_000, 1_000_000_000):
         sweep[str(pb)] = run("both", dict(base, prefetch_bucket_size=pb))[0]
+    paced = {"compute_only_ms": run("compute", paced=True)[0]}
+    for pb in (0, w.prefetch_bucket_size, 200_000_000):
+        paced["prefetch_" + str(pb) + "_ms"] = run("both", dict(base, prefetch_bucket_size=pb),
+                                                   paced=True)[0]
     ck = clocks.stop()
     gathered = 2 * sum(w.numel[p] for m in mods for p in m if not zs.zs_param_info(dw.plan, p)["persistent"])
     res = {"mode": "gather_schedule", "workload": w.name, "modules": len(mods),
@@ -746,7 +762,7 @@ def run_gather_schedule(args):
            "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
            "prefetch_overlapped_repeat_ms": t_over2, "no_prefetch_ms": t_serial, "clocks": ck,
            "prefetch_bucket_sweep_ms": sweep, "concurrency_probe": probe,
-           "by_gather_ctas": by_ctas,
+           "by_gather_ctas": by_ctas, "host_paced": paced,
            "hidden_fraction_of_gather": (t_comp + t_gath - t_over) / t_gath,
            "gathers_only_gbs": 2 * 2 * gathered / (t_gath * 1e-3) / 1e9 if t_gath else None,
            "sched_stats": st, "config": dict(base, arena_elems=arena_elems)}

@@ -69,7 +69,8 @@ typedef int32_t zs_status;
 #define ZS_ENOMEM   (-2)   /* host allocation failed                        */
 #define ZS_ECUDA    (-3)   /* a CUDA call failed (message names it)         */
 #define ZS_ESTATE   (-4)   /* call out of order (e.g. plan not uploaded)    */
-#define ZS_ETIMEOUT (-5)   /* reserved: no entry point waits on the device  */
+#define ZS_ETIMEOUT (-5)   /* a bounded device wait gave up (reported by
+                              zs_device_wait_timeouts)                     */
 
 /* Largest N the per-bucket reduce-scatter accepts (its rank pointers travel
  * as kernel arguments). */
@@ -391,9 +392,18 @@ zs_status zs_all_gather_coalesced(const zs_plan *plan, int32_t n, const int32_t 
  * per chunk; a wait that does not complete within a bound (about a second)
  * is abandoned, the gather's output is then incomplete, and this counter
  * goes up.  Synchronous (reads device memory).  reset != 0 sets it back to
- * 0.  Has no counterpart in the pages: it is this library's report of its
- * own bounded waits.  Errors: ZS_EINVAL (NULL count), ZS_ECUDA. */
+ * 0.  Returns ZS_ETIMEOUT, with *count filled, when the count is not 0.
+ * Has no counterpart in the pages: it is this library's report of its own
+ * bounded waits.  Errors: ZS_EINVAL (NULL count), ZS_ECUDA. */
 zs_status zs_device_wait_timeouts(int32_t *count, int32_t reset);
+
+/* Test hook for the timeout path: enqueues one thread that waits, with the
+ * bulk gather's bounded wait but a limit of limit_ns nanoseconds (0 <
+ * limit_ns <= 2e9), on an mbarrier that nothing arrives on.  The wait gives
+ * up, the count of zs_device_wait_timeouts goes up by one, and the CUDA
+ * context stays usable: nothing faults, traps or spins without bound.  Has
+ * no counterpart in the pages.  Errors: ZS_EINVAL (limit), ZS_ECUDA. */
+zs_status zs_test_wait_timeout(int64_t limit_ns, void *stream);
 
 /* A2 over every bucket in one launch — the first pass of zs_shard_step.
  * Same result as zs_reduce_scatter on each bucket in turn.  d_rank_grads

@@ -246,3 +246,10 @@ def test_device_calls_reject_bad_arguments_before_any_launch():
         zs.zs_all_gather_coalesced(plan2, [0], 16, 16, 100)
     with pytest.raises(zs.ZsError):
         zs.zs_grad_norm(plan2, None, None, None, False, 1.0, 16, 16, 16)
+
+
+def test_wait_timeout_hook_checks_its_limit():
+    for bad in (0, -1, 2_000_000_001):
+        with pytest.raises(zs.ZsError) as ei:
+            zs.zs_test_wait_timeout(bad)
+        assert ei.value.status == zs.ZS_EINVAL

@@ -149,6 +149,7 @@ _sig("zs_adam_step", _i32, [_P, _i32, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                             C.POINTER(zs_shard_state), _P])
 _sig("zs_all_gather_coalesced", _i32, [_P, _i32, C.POINTER(_i32), _P, _P, _i64, C.POINTER(_i64), _P])
 _sig("zs_device_wait_timeouts", _i32, [C.POINTER(_i32), _i32])
+_sig("zs_test_wait_timeout", _i32, [_i64, _P])
 _sig("zs_reduce_scatter_all", _i32, [_P, _P, _P, _P, _P, _P])
 _sig("zs_adam_gather", _i32, [_P, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                               C.POINTER(zs_shard_state), _P, _P])
@@ -389,8 +390,15 @@ def zs_all_gather_coalesced(plan, params, param_shards, flat_out, flat_capacity:
 def zs_device_wait_timeouts(reset: bool = False) -> int:
     """Bounded device waits that gave up on the current device (synchronous)."""
     c = _i32()
-    _check(_lib.zs_device_wait_timeouts(C.byref(c), int(bool(reset))), "zs_device_wait_timeouts")
+    st = _lib.zs_device_wait_timeouts(C.byref(c), int(bool(reset)))
+    if st != ZS_ETIMEOUT:
+        _check(st, "zs_device_wait_timeouts")
     return c.value
+
+
+def zs_test_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Enqueue one bounded wait that runs out after limit_ns (test hook)."""
+    _check(_lib.zs_test_wait_timeout(int(limit_ns), _stream(stream)), "zs_test_wait_timeout")
 
 
 def zs_shard_step(plan, d_rank_grads, state: zs_shard_state, norm_scratch, hp, step: int,

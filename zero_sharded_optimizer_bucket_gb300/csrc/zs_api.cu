@@ -271,8 +271,17 @@ zs_status zs_device_wait_timeouts(int32_t *count, int32_t reset) {
     const cudaError_t e = zsl_bulk_wait_timeouts(&c, reset != 0);
     if (e != cudaSuccess) return cuda_status(e, "zs_device_wait_timeouts");
     *count = c;
+    if (c != 0)
+        return zs_fail(ZS_ETIMEOUT, "zs_device_wait_timeouts: %d bounded device wait(s) gave up", c);
     zs_clear_error();
     return ZS_OK;
+}
+
+zs_status zs_test_wait_timeout(int64_t limit_ns, void *stream) {
+    if (limit_ns <= 0 || limit_ns > 2000000000ll)
+        return zs_fail(ZS_EINVAL, "zs_test_wait_timeout: limit_ns %lld not in (0, 2e9]",
+                       (long long)limit_ns);
+    return cuda_status(zsl_wait_timeout_test(limit_ns, (cudaStream_t)stream), "zs_test_wait_timeout");
 }
 
 zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *params,

@@ -92,7 +92,7 @@ constexpr int BULK_CHUNK = ZS_BULK_CHUNK;              // bytes per chunk (multi
 constexpr int64_t BULK_CHUNK_ELEMS = BULK_CHUNK / 2;
 constexpr int BULK_SMEM = BULK_STAGES * BULK_CHUNK;
 constexpr int BULK_SMEM_ALLOC = BULK_SMEM + 8 * BULK_STAGES;   // + mbarriers
-constexpr long long BULK_WAIT_LIMIT = 1ll << 22;       // try_wait calls per wait
+constexpr uint64_t BULK_WAIT_NS = 1000000000ull;       // one wait gives up after 1 s
 
 __device__ int g_bulk_wait_timeouts;                    // waits that gave up
 
@@ -100,8 +100,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (long long i = 0; i < BULK_WAIT_LIMIT; ++i) {
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of parity `parity` of the mbarrier at shared address
+// bar to complete; false when limit_ns pass first (the clock is read every
+// 64 polls; a poll count far beyond any such time is a second bound).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    for (long long i = 0; i < (1ll << 34); ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -111,6 +121,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((i & 63) == 63 && global_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
@@ -188,7 +199,7 @@ gather_bulk_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t
     bool ok = true;
     for (int64_t k = 0; k < mine; ++k) {
         const int s = (int)(k % BULK_STAGES);
-        if (!mbar_wait(bar(s), (uint32_t)((k / BULK_STAGES) & 1))) {
+        if (!mbar_wait(bar(s), (uint32_t)((k / BULK_STAGES) & 1), BULK_WAIT_NS)) {
             ok = false;
             break;
         }
@@ -214,10 +225,22 @@ gather_bulk_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t
         for (int64_t k = 0; k < issued; ++k) {
             const int s = (int)(k % BULK_STAGES);
             if (k + BULK_STAGES < issued) continue;
-            mbar_wait(bar(s), (uint32_t)((k / BULK_STAGES) & 1));
+            mbar_wait(bar(s), (uint32_t)((k / BULK_STAGES) & 1), BULK_WAIT_NS);
         }
     }
     asm volatile("cp.async.bulk.wait_group 0;" : : : "memory");
+}
+
+// One thread waits, with the bulk gather's bounded wait, on an mbarrier
+// that nothing arrives on: the wait gives up after limit_ns and counts one
+// timeout, as a stuck bulk copy would.
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" : : "r"(b) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" : : : "memory");
+    if (!mbar_wait(b, 0, limit_ns)) atomicAdd(&g_bulk_wait_timeouts, 1);
 }
 
 }  // namespace zsk
@@ -291,4 +314,9 @@ cudaError_t zsl_bulk_wait_timeouts(int *count, bool reset) {
         e = cudaMemcpyToSymbol(g_bulk_wait_timeouts, &zero, sizeof(int));
     }
     return e;
+}
+
+cudaError_t zsl_wait_timeout_test(int64_t limit_ns, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>((uint64_t)limit_ns);
+    return cudaGetLastError();
 }

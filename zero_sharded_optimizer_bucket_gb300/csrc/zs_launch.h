@@ -65,3 +65,5 @@ cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *
                        cudaStream_t s, int max_ctas);
 // Number of bounded waits of the bulk gather that gave up (synchronous).
 cudaError_t zsl_bulk_wait_timeouts(int *count, bool reset);
+// One bounded wait on an mbarrier nothing arrives on (gives up after limit_ns).
+cudaError_t zsl_wait_timeout_test(int64_t limit_ns, cudaStream_t s);
