@@ -519,6 +519,7 @@ def run_gpu(args):
                    "parallelism": "replicas" if world > 1 else "single GPU, N virtual ranks"},
         "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
         "hbm_frac_of_measured": step_bytes / (step_ms * 1e-3) / 1e9 / peak,
+        "hbm_frac_of_nominal_7900": step_bytes / (step_ms * 1e-3) / 1e9 / 7900.0,
         "kernel_ms": avg,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,

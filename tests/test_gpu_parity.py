@@ -41,6 +41,9 @@ CASES = {
     "numel_lt_n": dict(numel=[1, 2, 3, 5, 0, 9, 17], N=16, threshold=0),
     "n1": dict(numel=[100, 7, 4099, 1], N=1, threshold=5, B=2048),
     "many_small_64": dict(numel=workloads.many_small(60).numel, N=64, threshold=100_000),
+    # the largest rank count the library takes (ZS_MAX_RANKS): 256 rank
+    # buffers per bucket, most parameters smaller than N
+    "n256_max_ranks": dict(_ragged(9, n=14, N=256), B=4000, threshold=20),
     # partition sizes multiples of 8 and >= 1024: gathers into a 16-byte
     # aligned buffer take the bulk-copy path, many 32 KB chunks long; the
     # 70001-element parameter sends any request holding it to the other path

@@ -23,26 +23,33 @@ from tests.test_sched_host import _oracle_records  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("seed,N,arena_factor,prefetch,ctas,aligned",
-                         [(1, 4, 2.0, 30000, 0, False), (2, 8, 1.3, 5000, 1, False),
-                          (3, 3, 4.0, 100000, 3, False), (4, 16, 1.1, 0, 0, False),
-                          (5, 5, 1.5, 20000, 152, False), (6, 4, 1.5, 30000, 0, True),
-                          (7, 2, 1.3, 60000, 2, True)])
-def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas, aligned):
+@pytest.mark.parametrize("seed,N,arena_factor,prefetch,ctas,aligned,group,dtype",
+                         [(1, 4, 2.0, 30000, 0, False, 0, "bf16"),
+                          (2, 8, 1.3, 5000, 1, False, 0, "bf16"),
+                          (3, 3, 4.0, 100000, 3, False, 0, "bf16"),
+                          (4, 16, 1.1, 0, 0, False, 0, "bf16"),
+                          (5, 5, 1.5, 20000, 152, False, 0, "bf16"),
+                          (6, 4, 1.5, 30000, 0, True, 0, "bf16"),
+                          (7, 2, 1.3, 60000, 2, True, 0, "bf16"),
+                          (8, 8, 1.5, 30000, 0, False, 2, "bf16"),
+                          (9, 8, 1.5, 30000, 152, True, 4, "fp16")])
+def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas, aligned, group,
+                                       dtype):
     """ctas caps the gather grid (strided loops cover the rest).  aligned:
     partition sizes are multiples of 8 and >= 1024, so every block of the
     arena starts on a 16-byte boundary and the gathers take the bulk-copy
-    path."""
+    path.  group: HSDP shard groups (a gather assembles G shards)."""
     rng = np.random.default_rng(seed)
+    G = group or N
     if aligned:
-        numel = [8 * N * int(x) for x in rng.integers(128, 2500 // N + 130, size=30)]
+        numel = [8 * G * int(x) for x in rng.integers(128, 2500 // G + 130, size=30)]
     else:
         numel = [int(x) for x in rng.integers(1, 20000, size=30)]
-    d = H.DevicePlan(numel, N, threshold=200, seed=seed)
+    d = H.DevicePlan(numel, N, threshold=200, seed=seed, group=group, dtype=dtype)
     d.init_weights()
     expect = ostep.gather_model(d.op, d.ost.param_shards)
     mods = [[int(x) for x in rng.integers(0, 30, size=int(rng.integers(1, 5)))] for _ in range(14)]
-    largest = max(sum(N * d.op.params[p].ps for p in set(m)) for m in mods)
+    largest = max(sum(G * d.op.params[p].ps for p in set(m)) for m in mods)
     # the arena holds the live budget (plus padding) and the largest module,
     # with arena_factor of slack for fragmentation
     cfg = dict(prefetch_bucket_size=prefetch, max_live_parameters=60000,
