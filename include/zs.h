@@ -18,7 +18,9 @@
  *   returns ZS_ECUDA.  No call aborts or exits; zs_last_error() gives a
  *   message for the calling thread.
  * - Device buffers are owned by the caller; the library allocates no device
- *   memory.  The plan is host memory owned by the library (zs_free_plan).
+ *   memory (its only device memory is static: the scratch array of
+ *   zs_grad_norm_noalloc and a counter of timed-out waits).  The plan is
+ *   host memory owned by the library (zs_free_plan).
  * - Device work is enqueued on the caller's cudaStream_t (passed as void*,
  *   NULL = legacy default stream).  No call synchronises the host with the
  *   device; results such as the gradient norm stay in device memory.
