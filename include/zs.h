@@ -499,10 +499,13 @@ typedef struct {
     int64_t max_reuse_distance;     /* elements, e.g. 1e9                     */
     int64_t arena_elems;            /* capacity of the arena                  */
     int64_t gather_ctas;            /* CTAs per gather launch, 0..2^20: 0 lets
-                                       a gather take the whole GPU; a cap
+                                       a gather take the whole GPU (its CTAs
+                                       queued behind one another then delay
+                                       the compute stream's kernels); a cap
                                        (e.g. 152, one per SM) leaves room for
-                                       the compute stream's kernels, as a
-                                       collective's few channels would      */
+                                       them, as a collective's few channels
+                                       would; the bulk-copy path still moves
+                                       about 6 TB/s with one CTA per SM     */
 } zs_sched_config;
 
 typedef struct {

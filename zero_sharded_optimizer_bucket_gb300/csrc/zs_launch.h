@@ -60,7 +60,7 @@ struct ZsGatherArgs {
     int64_t out_lo, out_hi;
 };
 
-// max_ctas caps the grid (0: one wave of resident CTAs)
+// max_ctas caps the grid (0: the default, 8 CTAs per SM on either path)
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
                        cudaStream_t s, int max_ctas);
 // Number of bounded waits of the bulk gather that gave up (synchronous).
