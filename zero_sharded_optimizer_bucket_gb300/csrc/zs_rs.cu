@@ -27,6 +27,12 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     __shared__ const uint16_t *sp[ZS_MAX_RANKS];
     __shared__ double red[WARPS];
     __shared__ int bad;
+    // Launched as a programmatic dependent: wait until the previous kernel
+    // of the stream has finished and its writes are visible (a no-op in an
+    // ordinary launch), then let the next dependent launch start placing
+    // its CTAs, which wait the same way.
+    asm volatile("griddepcontrol.wait;" : : : "memory");
+    asm volatile("griddepcontrol.launch_dependents;" : : : "memory");
     const int64_t t = tile0 + blockIdx.x;
     const ZsTile tile = tiles[t];
     if (threadIdx.x == 0) bad = 0;
@@ -285,20 +291,43 @@ norm_finish_kernel(const double *__restrict__ level1, int64_t n1, float max_norm
 
 using namespace zsk;
 
+// Per-bucket launches go out as programmatic dependents of the previous
+// kernel in the stream: back-to-back buckets then lose the launch gap
+// between them.  Stream order is kept: each CTA first waits for the
+// previous kernel (griddepcontrol.wait in rs_kernel).
+template <bool FROM_TABLE, class T, bool GROUPED>
+static cudaError_t launch_rs_pdl(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+                                 const RankPtrs &p, const uint16_t *const *tbl, int N, int G,
+                                 uint16_t *gs, uint16_t *gP, double *partials, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ntiles);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rs_kernel<FROM_TABLE, T, GROUPED>, d_tiles, tile0, p, tbl, N, G,
+                              (float)N, gs, gP, partials);
+}
+
 template <class T>
 static cudaError_t launch_rs(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
                              const RankPtrs &p, const void *const *d_table, int N, int G, uint16_t *gs,
                              uint16_t *gP, double *partials, cudaStream_t s) {
     const auto *tbl = reinterpret_cast<const uint16_t *const *>(d_table);
     const dim3 g((unsigned)ntiles), b(THREADS);
-    if (G == N) {
-        if (d_table) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
-        else rs_kernel<false, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, nullptr, N, G, (float)N, gs, gP, partials);
-    } else {
-        if (d_table) rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
-        else rs_kernel<false, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, nullptr, N, G, (float)N, gs, gP, partials);
+    if (d_table) {
+        if (G == N) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
+        else rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    const cudaError_t e =
+        G == N ? launch_rs_pdl<false, T, false>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s)
+               : launch_rs_pdl<false, T, true>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
