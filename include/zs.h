@@ -506,6 +506,9 @@ typedef struct {
                                        them, as a collective's few channels
                                        would; the bulk-copy path still moves
                                        about 6 TB/s with one CTA per SM     */
+    int64_t log_limit;              /* log records kept, the most recent ones:
+                                       0 = 2^20, -1 = all (grows with every
+                                       pass), n > 0 = n                     */
 } zs_sched_config;
 
 typedef struct {
@@ -550,7 +553,8 @@ zs_status zs_sched_end_pass(zs_sched *sched, void *compute_stream);
  * Errors: ZS_EINVAL (index), ZS_ESTATE (not gathered now). */
 zs_status zs_sched_param_offset(const zs_sched *sched, int32_t param, int64_t *offset);
 zs_status zs_sched_stats(const zs_sched *sched, zs_sched_stats_t *out);
-/* Copy up to cap log records; *n receives the total count. */
+/* Copy up to cap of the kept log records (oldest first); *n receives how
+ * many are kept (at most log_limit). */
 zs_status zs_sched_log(const zs_sched *sched, zs_sched_event *out, int64_t cap, int64_t *n);
 
 #ifdef __cplusplus

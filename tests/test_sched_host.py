@@ -188,3 +188,28 @@ def test_gather_cta_cap_is_checked():
             zs.zs_sched_create(plan_c, [[0], [1]], dict(base, gather_ctas=bad))
         assert ei.value.status == zs.ZS_EINVAL
     assert zs.zs_sched_create(plan_c, [[0], [1]], dict(base, gather_ctas=152)).handle
+
+
+def test_log_keeps_the_most_recent_records():
+    numel = [5000, 7000, 3000]
+    plan_c = zs.zs_build_partition(zs.zs_default_config(2), numel)
+    base = dict(prefetch_bucket_size=8000, max_live_parameters=100000, max_reuse_distance=0,
+                arena_elems=40000)
+    mods = [[0], [1, 2], [0]]
+
+    def run(limit):
+        c = zs.zs_sched_create(plan_c, mods, dict(base, log_limit=limit))
+        for _ in range(5):
+            for m in range(3):
+                zs.zs_sched_fetch(c, m)
+                zs.zs_sched_release(c, m)
+            zs.zs_sched_end_pass(c)
+        return zs.zs_sched_log(c)
+
+    full = run(-1)
+    assert run(0) == full                      # the default keeps 2^20 records
+    assert len(full) > 20
+    assert run(7) == full[-7:]
+    with pytest.raises(zs.ZsError) as ei:
+        zs.zs_sched_create(plan_c, mods, dict(base, log_limit=-2))
+    assert ei.value.status == zs.ZS_EINVAL

@@ -100,7 +100,7 @@ class zs_shard_state(C.Structure):
 class zs_sched_config(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("prefetch_bucket_size", "max_live_parameters",
                                          "max_reuse_distance", "arena_elems",
-                                         "gather_ctas")]
+                                         "gather_ctas", "log_limit")]
 
 
 class zs_sched_stats_t(C.Structure):

@@ -5,6 +5,7 @@
 // events (a gather's output is waited for by the module that uses it; a
 // gather that reuses released arena space waits for that release).
 #include <algorithm>
+#include <deque>
 #include <new>
 #include <utility>
 #include <vector>
@@ -35,7 +36,8 @@ struct zs_sched {
     std::vector<int32_t> producer;
     std::vector<Seg> free_;
     int64_t live = 0, ops = 0, releases = 0, arena_used = 0;
-    std::vector<zs_sched_event> log;
+    std::deque<zs_sched_event> log;     // the most recent records (log_limit)
+    int64_t log_cap = 0;                  // < 0: unlimited
     std::vector<cudaEvent_t> op_ev, rel_ev;
     zs_sched_stats_t st{};
 };
@@ -119,6 +121,12 @@ void free_seg(zs_sched *s, int32_t p, int64_t rel) {
     s->offset[p] = -1;
 }
 
+// Appends a log record, dropping the oldest beyond the log limit.
+void log_event(zs_sched *s, const zs_sched_event &e) {
+    s->log.push_back(e);
+    if (s->log_cap >= 0 && (int64_t)s->log.size() > s->log_cap) s->log.pop_front();
+}
+
 zs_status cuda_err(cudaError_t e, const char *what) {
     return zs_fail(ZS_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
@@ -151,7 +159,7 @@ zs_status gather(zs_sched *s, std::vector<int32_t> params, int64_t pos, const vo
         s->live += numel(s, p);
         elems += numel(s, p);
         block += psize(s, p);
-        s->log.push_back(zs_sched_event{1, (int32_t)pos, (int32_t)op, p, offs[i], waits});
+        log_event(s, zs_sched_event{1, (int32_t)pos, (int32_t)op, p, offs[i], waits});
     }
     s->arena_used += block;
     s->st.gathers += 1;
@@ -276,7 +284,8 @@ zs_status zs_sched_create(const zs_plan *P, int32_t n_modules, const int32_t *mo
         return zs_fail(ZS_EINVAL, "%s: bad arguments", fn);
     *out = nullptr;
     if (cfg->prefetch_bucket_size < 0 || cfg->max_live_parameters < 0 || cfg->max_reuse_distance < 0 ||
-        cfg->arena_elems < 0 || cfg->gather_ctas < 0 || cfg->gather_ctas > (1 << 20))
+        cfg->arena_elems < 0 || cfg->gather_ctas < 0 || cfg->gather_ctas > (1 << 20) ||
+        cfg->log_limit < -1)
         return zs_fail(ZS_EINVAL, "%s: negative size in the configuration", fn);
     if (d_arena && (reinterpret_cast<uintptr_t>(d_arena) & 15))
         return zs_fail(ZS_EINVAL, "%s: arena not 16-byte aligned", fn);
@@ -286,6 +295,7 @@ zs_status zs_sched_create(const zs_plan *P, int32_t n_modules, const int32_t *mo
     try {
         s->P = P;
         s->cfg = *cfg;
+        s->log_cap = cfg->log_limit == 0 ? (int64_t)1 << 20 : cfg->log_limit;
         s->arena = static_cast<uint16_t *>(d_arena);
         s->modules.resize(n_modules);
         s->module_numel.assign(n_modules, 0);
@@ -362,9 +372,9 @@ zs_status zs_sched_fetch(zs_sched *s, int32_t m, const void *shards, void *cstre
         if (s->live_flag[p] && std::find(ops.begin(), ops.end(), s->producer[p]) == ops.end())
             ops.push_back(s->producer[p]);
     std::sort(ops.begin(), ops.end());
-    if (ops.empty()) s->log.push_back(zs_sched_event{2, (int32_t)pos, -1, -1, 0, 0});
+    if (ops.empty()) log_event(s, zs_sched_event{2, (int32_t)pos, -1, -1, 0, 0});
     for (int32_t op : ops) {
-        s->log.push_back(zs_sched_event{2, (int32_t)pos, op, -1, 0, 0});
+        log_event(s, zs_sched_event{2, (int32_t)pos, op, -1, 0, 0});
         if (s->arena) {
             const cudaError_t e = cudaStreamWaitEvent((cudaStream_t)cstream, s->op_ev[op], 0);
             if (e != cudaSuccess) return cuda_err(e, "zs_sched_fetch: cudaStreamWaitEvent");
@@ -391,10 +401,10 @@ zs_status zs_sched_release(zs_sched *s, int32_t m, void *cstream) {
         if (!s->live_flag[p]) continue;
         if (s->complete && !s->invalid && reused_soon(s, p, pos)) continue;
         drop(s, p, rel);
-        s->log.push_back(zs_sched_event{3, (int32_t)pos, -1, p, 0, rel});
+        log_event(s, zs_sched_event{3, (int32_t)pos, -1, p, 0, rel});
         any = true;
     }
-    if (!any) s->log.push_back(zs_sched_event{3, (int32_t)pos, -1, -1, 0, rel});
+    if (!any) log_event(s, zs_sched_event{3, (int32_t)pos, -1, -1, 0, rel});
     zs_clear_error();
     return ZS_OK;
 }
@@ -410,9 +420,9 @@ zs_status zs_sched_end_pass(zs_sched *s, void *cstream) {
     sort_ds(s, out);
     for (int32_t p : out) {
         drop(s, p, rel);
-        s->log.push_back(zs_sched_event{3, (int32_t)s->pos, -1, p, 0, rel});
+        log_event(s, zs_sched_event{3, (int32_t)s->pos, -1, p, 0, rel});
     }
-    if (out.empty()) s->log.push_back(zs_sched_event{3, (int32_t)s->pos, -1, -1, 0, rel});
+    if (out.empty()) log_event(s, zs_sched_event{3, (int32_t)s->pos, -1, -1, 0, rel});
     if (s->complete && !s->invalid && s->pos != (int64_t)s->trace.size()) {
         s->invalid = true;
         s->st.invalidations += 1;
