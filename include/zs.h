@@ -490,7 +490,12 @@ zs_status zs_shard_step_scaled(const zs_plan *plan, const void *const *d_rank_gr
  *   reuse distance keeps plus the largest module, with slack for first-fit
  *   fragmentation; a fetch that does not fit fails with ZS_ENOMEM.
  * Gathers are enqueued on the gather stream, which the compute stream waits
- * on through CUDA events; neither call blocks the host. */
+ * on through CUDA events; neither call blocks the host.  The first fetch of
+ * a pass also makes the gather stream wait for everything enqueued on the
+ * compute stream before it, so that gathers read shards rewritten between
+ * passes (the optimizer step; [ZeRO-3 chapter] §6.3) on that stream.  A
+ * scheduler uses one compute stream and one gather stream, fixed by its
+ * first fetch; a call with other streams fails with ZS_EINVAL. */
 typedef struct zs_sched zs_sched;   /* opaque, host memory + CUDA events */
 
 typedef struct {

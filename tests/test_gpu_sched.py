@@ -90,3 +90,57 @@ def test_scheduled_gathers_are_correct(seed, N, arena_factor, prefetch, ctas, al
     if prefetch:
         assert st["elems_prefetched"] > 0
     d.check_canaries()
+
+
+def test_shards_rewritten_between_passes_are_gathered():
+    """The caller rewrites the parameter shards on the compute stream between
+    passes, behind a long kernel; every gather of the next pass must read
+    the new shards (the first fetch of a pass waits for the compute
+    stream)."""
+    rng = np.random.default_rng(21)
+    N = 4
+    numel = [8 * N * int(x) for x in rng.integers(200, 2000, size=12)]
+    d = H.DevicePlan(numel, N, threshold=100, seed=21)
+    d.init_weights()
+    first = ostep.gather_model(d.op, d.ost.param_shards)
+    mods = [[0, 1], [2], [3, 4, 5], [6], [7, 8], [9, 10, 11], [0, 4]]
+    largest = max(sum(N * d.op.params[p].ps for p in set(m)) for m in mods)
+    cfg = dict(prefetch_bucket_size=200000, max_live_parameters=10**7, max_reuse_distance=0,
+               arena_elems=int(sum(N * p.ps for p in d.op.params) + 2 * largest), gather_ctas=152)
+    arena = torch.full((cfg["arena_elems"],), -1, dtype=torch.int16, device=d.dev)
+    sched = zs.zs_sched_create(d.plan, mods, cfg, arena)
+    comp, gath = torch.cuda.Stream(), torch.cuda.Stream()
+    sink = torch.zeros(4, device=d.dev)
+    # new weights for the second pass, partitioned on the compute stream
+    W2 = np.asarray(rng.standard_normal(d.op.input_elems), dtype=np.float32)
+    W2d = torch.from_numpy(W2).to(d.dev)
+    second = ostep.gather_model(d.op, ostep.partition(d.op, W2).param_shards)
+    torch.cuda.synchronize()
+
+    def one_pass(expect):
+        for m in range(len(mods)):
+            zs.zs_sched_fetch(sched, m, d.bufs["param_shards"].ptr(), comp, gath)
+            views = {}
+            for p in set(mods[m]):
+                off = zs.zs_sched_param_offset(sched, p)
+                q = d.op.params[p]
+                with torch.cuda.stream(comp):
+                    views[p] = arena[off:off + q.numel].clone()
+            zs.zs_sched_release(sched, m, comp)
+            comp.synchronize()
+            for p, v in views.items():
+                q = d.op.params[p]
+                assert np.array_equal(v.cpu().numpy().view(np.uint16),
+                                      expect[q.flat_off:q.flat_off + q.numel]), (m, p)
+        zs.zs_sched_end_pass(sched, comp)
+
+    one_pass(first)                     # records the trace
+    sgpu.busy(3_000_000, 152, sink, comp, 32)   # a long step on the compute stream ...
+    zs.zs_partition(d.plan, W2d, d.state, comp)  # ... that rewrites the shards
+    one_pass(second)                    # prefetching pass: must see the new shards
+    with pytest.raises(zs.ZsError) as ei:   # the streams are fixed
+        zs.zs_sched_fetch(sched, 0, d.bufs["param_shards"].ptr(), gath, comp)
+    assert ei.value.status == zs.ZS_EINVAL
+    torch.cuda.synchronize()
+    assert zs.zs_device_wait_timeouts() == 0
+    d.check_canaries()

@@ -38,7 +38,15 @@ struct zs_sched {
     int64_t live = 0, ops = 0, releases = 0, arena_used = 0;
     std::deque<zs_sched_event> log;     // the most recent records (log_limit)
     int64_t log_cap = 0;                  // < 0: unlimited
+    // CUDA events, pooled per pass: op_ev[op - pass_first_op] and
+    // rel_ev[rel - pass_first_rel].  The first fetch of a pass makes the
+    // gather stream wait for the compute stream (pass_ev), which covers
+    // every release recorded before it, so older events are never needed.
     std::vector<cudaEvent_t> op_ev, rel_ev;
+    cudaEvent_t pass_ev = nullptr;
+    int64_t pass_first_op = 0, pass_first_rel = 0;
+    void *cstream = nullptr, *gstream = nullptr;   // fixed at the first device call
+    bool streams_set = false;
     zs_sched_stats_t st{};
 };
 
@@ -171,8 +179,8 @@ zs_status gather(zs_sched *s, std::vector<int32_t> params, int64_t pos, const vo
     if (!s->arena) return ZS_OK;
     const cudaStream_t gs = (cudaStream_t)gstream;
     zs_status r;
-    if (waits >= 0) {
-        const cudaError_t e = cudaStreamWaitEvent(gs, s->rel_ev[waits], 0);
+    if (waits >= s->pass_first_rel) {      // older releases precede the pass-start wait
+        const cudaError_t e = cudaStreamWaitEvent(gs, s->rel_ev[waits - s->pass_first_rel], 0);
         if (e != cudaSuccess) return cuda_err(e, "zs_sched: cudaStreamWaitEvent");
     }
     std::vector<int64_t> views(params.size());
@@ -182,8 +190,8 @@ zs_status gather(zs_sched *s, std::vector<int32_t> params, int64_t pos, const vo
     for (size_t i = 0; i < params.size(); ++i)
         if (views[i] != offs[i] - offs[0])
             return zs_fail(ZS_ESTATE, "zs_sched: gather layout mismatch (internal)");
-    if ((r = ensure_event(s->op_ev, op))) return r;
-    const cudaError_t e = cudaEventRecord(s->op_ev[op], gs);
+    if ((r = ensure_event(s->op_ev, op - s->pass_first_op))) return r;
+    const cudaError_t e = cudaEventRecord(s->op_ev[op - s->pass_first_op], gs);
     if (e != cudaSuccess) return cuda_err(e, "zs_sched: cudaEventRecord");
     return ZS_OK;
 }
@@ -256,10 +264,28 @@ void drop(zs_sched *s, int32_t p, int64_t rel) {
 
 zs_status record_release(zs_sched *s, int64_t rel, void *cstream) {
     if (!s->arena) return ZS_OK;
-    zs_status r = ensure_event(s->rel_ev, rel);
+    zs_status r = ensure_event(s->rel_ev, rel - s->pass_first_rel);
     if (r) return r;
-    const cudaError_t e = cudaEventRecord(s->rel_ev[rel], (cudaStream_t)cstream);
+    const cudaError_t e = cudaEventRecord(s->rel_ev[rel - s->pass_first_rel], (cudaStream_t)cstream);
     return e == cudaSuccess ? ZS_OK : cuda_err(e, "zs_sched: cudaEventRecord");
+}
+
+// The scheduler's streams are fixed by its first device call; every later
+// call must pass the same ones (gstream NULL: not checked, the call has none).
+zs_status check_streams(zs_sched *s, void *cstream, void *gstream, bool has_gather,
+                        const char *fn) {
+    if (!s->arena) return ZS_OK;
+    if (!s->streams_set) {
+        if (!has_gather) return ZS_OK;      // fixed by the first fetch
+        s->cstream = cstream;
+        s->gstream = gstream;
+        s->streams_set = true;
+        return ZS_OK;
+    }
+    if (cstream != s->cstream || (has_gather && gstream != s->gstream))
+        return zs_fail(ZS_EINVAL,
+                       "%s: the compute and gather streams must be the same in every call", fn);
+    return ZS_OK;
 }
 
 void build_queue(zs_sched *s) {
@@ -340,6 +366,7 @@ void zs_sched_destroy(zs_sched *s) {
     if (!s) return;
     for (cudaEvent_t e : s->op_ev) cudaEventDestroy(e);
     for (cudaEvent_t e : s->rel_ev) cudaEventDestroy(e);
+    if (s->pass_ev) cudaEventDestroy(s->pass_ev);
     delete s;
 }
 
@@ -350,6 +377,22 @@ zs_status zs_sched_fetch(zs_sched *s, int32_t m, const void *shards, void *cstre
         return zs_fail(ZS_EINVAL, "%s: module %d out of range", fn, m);
     if (s->arena && s->P->S > 0 && (!shards || (reinterpret_cast<uintptr_t>(shards) & 15)))
         return zs_fail(ZS_EINVAL, "%s: param_shards NULL or not 16-byte aligned", fn);
+    zs_status r = check_streams(s, cstream, gstream, true, fn);
+    if (r) return r;
+    if (s->pos == 0) {
+        // a new pass: its gathers read shards that the caller may have
+        // rewritten (the optimizer step) on the compute stream since the
+        // last pass, so the gather stream waits for the compute stream here
+        s->pass_first_op = s->ops;
+        s->pass_first_rel = s->releases;
+        if (s->arena) {
+            cudaError_t e = cudaSuccess;
+            if (!s->pass_ev) e = cudaEventCreateWithFlags(&s->pass_ev, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventRecord(s->pass_ev, (cudaStream_t)cstream);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent((cudaStream_t)gstream, s->pass_ev, 0);
+            if (e != cudaSuccess) return cuda_err(e, "zs_sched_fetch: pass-start wait");
+        }
+    }
     const int64_t pos = s->pos++;
     if (s->complete && !s->invalid && (pos >= (int64_t)s->trace.size() || s->trace[pos] != m)) {
         s->invalid = true;
@@ -359,7 +402,6 @@ zs_status zs_sched_fetch(zs_sched *s, int32_t m, const void *shards, void *cstre
     std::vector<int32_t> need;
     for (int32_t p : dedup(s->modules[m]))
         if (gatherable(s, p) && !s->live_flag[p]) need.push_back(p);
-    zs_status r;
     if (!need.empty()) {
         r = gather(s, need, pos, shards, gstream, false);
         if (r == ZS_ENOMEM)
@@ -376,7 +418,8 @@ zs_status zs_sched_fetch(zs_sched *s, int32_t m, const void *shards, void *cstre
     for (int32_t op : ops) {
         log_event(s, zs_sched_event{2, (int32_t)pos, op, -1, 0, 0});
         if (s->arena) {
-            const cudaError_t e = cudaStreamWaitEvent((cudaStream_t)cstream, s->op_ev[op], 0);
+            const cudaError_t e =
+                cudaStreamWaitEvent((cudaStream_t)cstream, s->op_ev[op - s->pass_first_op], 0);
             if (e != cudaSuccess) return cuda_err(e, "zs_sched_fetch: cudaStreamWaitEvent");
         }
     }
@@ -392,9 +435,11 @@ zs_status zs_sched_release(zs_sched *s, int32_t m, void *cstream) {
     if (!s) return zs_fail(ZS_EINVAL, "%s: NULL scheduler", fn);
     if (m < 0 || m >= (int32_t)s->modules.size())
         return zs_fail(ZS_EINVAL, "%s: module %d out of range", fn, m);
+    zs_status r = check_streams(s, cstream, nullptr, false, fn);
+    if (r) return r;
     const int64_t pos = s->pos - 1;
     const int64_t rel = s->releases++;
-    zs_status r = record_release(s, rel, cstream);
+    r = record_release(s, rel, cstream);
     if (r) return r;
     bool any = false;
     for (int32_t p : dedup(s->modules[m])) {
@@ -411,8 +456,10 @@ zs_status zs_sched_release(zs_sched *s, int32_t m, void *cstream) {
 
 zs_status zs_sched_end_pass(zs_sched *s, void *cstream) {
     if (!s) return zs_fail(ZS_EINVAL, "zs_sched_end_pass: NULL scheduler");
+    zs_status r = check_streams(s, cstream, nullptr, false, "zs_sched_end_pass");
+    if (r) return r;
     const int64_t rel = s->releases++;
-    zs_status r = record_release(s, rel, cstream);
+    r = record_release(s, rel, cstream);
     if (r) return r;
     std::vector<int32_t> out;
     for (int32_t p = 0; p < (int32_t)s->live_flag.size(); ++p)
