@@ -253,3 +253,22 @@ def test_wait_timeout_hook_checks_its_limit():
         with pytest.raises(zs.ZsError) as ei:
             zs.zs_test_wait_timeout(bad)
         assert ei.value.status == zs.ZS_EINVAL
+
+
+def test_parameter_larger_than_2_to_32_elements():
+    """Offsets, chunk buckets and tiles of a parameter of 2^33 + 5 elements
+    (beyond any 32-bit index), next to small ones: the plan equals the
+    oracle's and its tiles cover every destination element once."""
+    numel = [3000, 2 ** 33 + 5, 77, 2 ** 20 + 1]
+    op, cp = _compare(numel, 16, threshold=100, B=50_000_000, G=60_000_000, U=2 ** 31)
+    info = zs.zs_plan_info(cp)
+    big = zs.zs_param_info(cp, 1)
+    ps = -(-(2 ** 33 + 5) // 16)
+    assert big["partition_size"] == ps and big["padding"] == 16 * ps - (2 ** 33 + 5)
+    assert big["n_reduce_buckets"] == -(-(2 ** 33 + 5) // 50_000_000)
+    assert info["flat_elems"] == sum(16 * -(-n // 16) for n in numel if n >= 100)
+    tiles = zs.zs_plan_table(cp)
+    part = tiles[tiles["flat"] >= 0]
+    # every shard row of every partitioned parameter is tiled exactly once
+    assert int(part["len"].astype(np.int64).sum()) == 16 * info["shard_elems"]
+    assert int(tiles["valid"].astype(np.int64).sum()) == info["psi"]
