@@ -185,6 +185,16 @@ def llama3_8b_hsdp() -> Workload:
     return w
 
 
+def giant_param() -> Workload:
+    """One parameter of 2^31 + 5 elements (past any 32-bit element index)
+    beside two small ones, N=2: an edge case of the kernels' index
+    arithmetic, about 50 GB on the device."""
+    shapes = [[2 ** 31 + 5], [4100], [64]]
+    names = ["giant", "small", "bias"]
+    return Workload("giant_param", 2, names, shapes, grad_sigma=1e-3, steps=1, max_norm=1.0,
+                    seed=0x5EED0009)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama_layer": llama_layer,
@@ -194,6 +204,7 @@ WORKLOADS = {
     "llama3_attn": llama3_attn,
     "llama3_8b_fp16": llama3_8b_fp16,
     "llama3_8b_hsdp": llama3_8b_hsdp,
+    "giant_param": giant_param,
 }
 
 

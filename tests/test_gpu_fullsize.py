@@ -92,7 +92,7 @@ def _locate(op, w, dw, cols, ranks):
 
 
 @pytest.mark.parametrize("name", ["llama_layer", "many_small", "llama3_16_layers", "llama3_8b",
-                                  "llama3_8b_fp16", "llama3_8b_hsdp"])
+                                  "llama3_8b_fp16", "llama3_8b_hsdp", "giant_param"])
 def test_fullsize_sampled(name):
     w = workloads.WORKLOADS[name]()
     op = _oracle_plan(w)
