@@ -682,34 +682,64 @@ def run_gather_schedule(args):
     arena_elems = base["max_live_parameters"] + 2 * largest
     arena = torch.empty(arena_elems, dtype=torch.int16, device=dev)
     sink = torch.zeros(4, device=dev)
-    comp, gath = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    # stand-in compute: one warp per SM running a dependent FMA chain takes
-    # time without taking the SMs' issue slots or memory bandwidth (as
-    # tensor-core compute leaves them); calibrate its ns per step
-    blocks, threads = 152, 32
+    # optionally a high-priority gather stream (freed SM slots then go to
+    # pending gather CTAs first, as collectives' streams are set up)
+    gprio = -1 if args.gather_priority == "high" else 0
+    comp, gath = torch.cuda.Stream(dev), torch.cuda.Stream(dev, priority=gprio)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sg.busy(10000, blocks, sink, comp, threads)
-    e0.record(comp)
-    sg.busy(200000, blocks, sink, comp, threads)
-    e1.record(comp)
-    torch.cuda.synchronize(dev)
-    ns_per_iter = e0.elapsed_time(e1) * 1e6 / 200000
-    # concurrency probe: the same compute beside one large gather on the other stream
+    if args.gather_compute == "gemm":
+        # stand-in compute: bf16 GEMMs (cuBLAS through torch) of tokens x
+        # 4096 by 4096 x 4096, as many per module as its parameters hold
+        # 4096^2 blocks: 2 * tokens * numel flops, with the shared memory,
+        # registers and tensor cores a real layer takes
+        X = torch.randn(args.tokens, 4096, device=dev, dtype=torch.bfloat16)
+        Wg = torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16) * 0.01
+        Y = torch.empty(args.tokens, 4096, device=dev, dtype=torch.bfloat16)
+        reps = [max(1, round(n / 4096 ** 2)) for n in mod_elems]
+
+        def compute(m, count=None):
+            with torch.cuda.stream(comp):
+                for _ in range(count if count is not None else reps[m]):
+                    torch.matmul(X, Wg, out=Y)
+        probe_count = 100
+        compute(None, 10)
+    else:
+        # stand-in compute: one warp per SM running a dependent FMA chain
+        # takes time without taking the SMs' issue slots or memory bandwidth
+        # (as tensor-core compute leaves them); calibrate its ns per step
+        blocks, threads = 152, 32
+        sg.busy(10000, blocks, sink, comp, threads)
+        e0.record(comp)
+        sg.busy(200000, blocks, sink, comp, threads)
+        e1.record(comp)
+        torch.cuda.synchronize(dev)
+        ns_per_iter = e0.elapsed_time(e1) * 1e6 / 200000
+        iters = [int(args.ns_per_elem * n / ns_per_iter) for n in mod_elems]
+
+        def compute(m, count=None):
+            sg.busy(count if count is not None else iters[m], blocks, sink, comp, threads)
+        probe_count = 200000
+    # concurrency probe: the same compute alone, then beside one large gather
+    # on the other stream
     probe_params = [p for p in range(len(w.numel))
                     if not zs.zs_param_info(dw.plan, p)["persistent"]][:8]
     pr_elems = sum(G * zs.zs_param_info(dw.plan, p)["partition_size"] for p in probe_params)
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     e0.record(comp)
-    sg.busy(200000, blocks, sink, comp, threads)
+    compute(None, probe_count)
+    e1.record(comp)
+    torch.cuda.synchronize(dev)
+    alone = e0.elapsed_time(e1)
+    e0.record(comp)
+    compute(None, probe_count)
     e1.record(comp)
     e2.record(gath)
     zs.zs_all_gather_coalesced(dw.plan, probe_params, dw.ps, arena, pr_elems, gath)
     e3.record(gath)
     torch.cuda.synchronize(dev)
-    probe = {"compute_ms_alone": ns_per_iter * 200000 / 1e6, "compute_ms_beside_gather":
-             e0.elapsed_time(e1), "gather_ms_beside_compute": e2.elapsed_time(e3)}
-    iters = [int(args.ns_per_elem * n / ns_per_iter) for n in mod_elems]
+    probe = {"compute_ms_alone": alone, "compute_ms_beside_gather": e0.elapsed_time(e1),
+             "gather_ms_beside_compute": e2.elapsed_time(e3)}
 
     def run(mode, cfg=None, passes=3, paced=False):
         """paced: the host waits for each module's compute before the next
@@ -726,7 +756,7 @@ def run_gather_schedule(args):
                 if sched:
                     zs.zs_sched_fetch(sched, m, dw.ps, comp, gath)
                 if mode != "gathers":
-                    sg.busy(iters[m], blocks, sink, comp, threads)
+                    compute(m)
                 if sched:
                     zs.zs_sched_release(sched, m, comp)
                 if paced:
@@ -769,7 +799,14 @@ def run_gather_schedule(args):
     gathered = 2 * sum(w.numel[p] for m in mods for p in m if not zs.zs_param_info(dw.plan, p)["persistent"])
     res = {"mode": "gather_schedule", "workload": w.name, "modules": len(mods),
            "passes": "forward + backward, " + str(len(order)) + " fetches",
-           "ns_per_elem_compute": args.ns_per_elem,
+           "compute": (f"bf16 GEMMs, {args.tokens} tokens x 4096 x 4096, "
+                       f"{sum(reps[m] for m in order)} per pass"
+                       if args.gather_compute == "gemm"
+                       else f"1 warp/SM FMA chain, {args.ns_per_elem} ns per element"),
+           "gather_stream_priority": args.gather_priority,
+           "compute_tflops": (2.0 * args.tokens * 4096 ** 2 * sum(reps[m] for m in order)
+                              / (t_comp * 1e-3) / 1e12 if args.gather_compute == "gemm"
+                              else None),
            "compute_only_ms": t_comp, "gathers_only_ms": t_gath, "prefetch_overlapped_ms": t_over,
            "prefetch_overlapped_repeat_ms": t_over2, "no_prefetch_ms": t_serial, "clocks": ck,
            "prefetch_bucket_sweep_ms": sweep, "concurrency_probe": probe,
@@ -793,6 +830,12 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--gather-schedule", action="store_true",
                     help="measure the forward/backward gather scheduler instead of the step")
+    ap.add_argument("--gather-compute", default="busy", choices=["busy", "gemm"],
+                    help="gather-schedule mode: the stand-in compute of a module")
+    ap.add_argument("--gather-priority", default="normal", choices=["high", "normal"],
+                    help="gather-schedule mode: priority of the gather stream")
+    ap.add_argument("--tokens", type=int, default=2048,
+                    help="gather-schedule mode with --gather-compute gemm: GEMM rows")
     ap.add_argument("--ns-per-elem", type=float, default=0.002,
                     help="stand-in compute per parameter element and pass (gather-schedule "
                          "mode); 0.002 ns is 6 flops x ~570 tokens at 1.7 PFLOP/s")
