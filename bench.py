@@ -424,15 +424,20 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
     comp = torch.cuda.current_stream(dw.dev)
     filled = [torch.cuda.Event() for _ in range(slots)]
     free = [torch.cuda.Event() for _ in range(slots)]
-    out = torch.empty(2, dtype=torch.int32, pin_memory=True)
+    # each step's result (norm bits, skip flags) is read back into its own
+    # pinned row; the host does not wait for it inside the step, so the next
+    # step's host->device copies overlap this step's update
+    out = torch.empty((steps + warmup + 1, 2), dtype=torch.int32, pin_memory=True)
     h2d = sum(2 * N * L for L in dw.buf_elems)
+    row = [0]
+    used = [False] * slots
 
     def one_step():
         dw.t += 1
         for b in range(nb):
             s = b % slots
             n = sizes[b]          # the N rank buffers of the bucket, back to back
-            if b >= slots:
+            if used[s]:           # the slot's last reader (this step or the last) is done
                 cs.wait_event(free[s])
             with torch.cuda.stream(cs):
                 ring[s * smax:s * smax + n].copy_(host[hoffs[b]:hoffs[b] + n], non_blocking=True)
@@ -442,11 +447,12 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
             ptrs = [base + 2 * k * _align8(dw.buf_elems[b]) for k in range(N)]
             zs.zs_reduce_scatter(dw.plan, b, ptrs, dw.gs, dw.gP, dw.scratch)
             free[s].record(comp)
+            used[s] = True
         dw.norm()
         zs.zs_adam_gather(dw.plan, dw.hp, dw.t, dw.d_coef, dw.d_flags, dw.state, dw.flat)
-        out[0:1].copy_(dw.d_norm[0:1].view(torch.int32), non_blocking=True)
-        out[1:2].copy_(dw.d_flags[0:1], non_blocking=True)
-        comp.synchronize()
+        out[row[0], 0:1].copy_(dw.d_norm[0:1].view(torch.int32), non_blocking=True)
+        out[row[0], 1:2].copy_(dw.d_flags[0:1], non_blocking=True)
+        row[0] += 1
 
     for _ in range(warmup):
         one_step()
@@ -469,16 +475,20 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
         return out
 
     rates = link_rates()
+    torch.cuda.synchronize(dw.dev)
     t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
+    torch.cuda.synchronize(dw.dev)       # every step's result is on the host
     dt = (time.perf_counter() - t0) / steps
+    flags = [int(out[i, 1]) for i in range(row[0])]
     rates += link_rates()
     link_gbs = max(rates)
     return {"value": dw.info["psi"] / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": 8, "ms_per_step": dt * 1e3, "steps": steps,
             "h2d_gbs_achieved": h2d / dt / 1e9, "h2d_link_gbs_measured": link_gbs,
             "h2d_link_gbs_range": [min(rates), max(rates)],
+            "skip_flags": flags,
             "path": "pinned host gradients -> per-bucket H2D ring -> zs_reduce_scatter; "
                     "zs_grad_norm; zs_adam_gather; norm+flags D2H"}
 
