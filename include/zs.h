@@ -28,10 +28,11 @@
  * - Device buffers read or written with 16-byte vectors must be 16-byte
  *   aligned: every buffer except the flat output of the gathers, which needs
  *   only 2-byte alignment.  Misalignment is ZS_EINVAL.
- * - A call's output buffers must not overlap its input buffers or one
- *   another (the rank gradients, the shards and the state of a step, the
- *   flat output of a gather); overlapping buffers give undefined results
- *   and are not detected.
+ * - Distinct buffers of a call must not overlap (rank gradients, gradient
+ *   shards, parameter shards, each state buffer, the persistent buffers, the
+ *   flat output, scratch); a buffer the call updates in place (the fp32
+ *   master and moments) is one buffer, read and written.  Overlapping
+ *   buffers give undefined results and are not detected.
  *
  * Layouts (elements; "ds_id order" = parameters sorted by ds_id)
  * --------------------------------------------------------------
