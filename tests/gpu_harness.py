@@ -7,7 +7,7 @@ sanitizer).  Inputs come from the shared generator `synth` only (the CPU
 implementation, or the GPU one for larger inputs, which
 test_gpu_parity.test_generator_gpu_matches_cpu pins to the CPU one).
 
-Tolerances (the benchmark spec, written out):
+Tolerances (the parity targets of the method, written out):
   reduce-scatter, partition, gather : bit-exact
   gradient norm                     : |a - b| <= 1e-5 |b|
   fp32 master / exp_avg / exp_avg_sq: |a - b| <= 1e-6 (|b| + mean|b|) — relative
