@@ -457,7 +457,7 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
     for _ in range(warmup):
         one_step()
     torch.cuda.synchronize(dw.dev)
-    # the box's own host->device rate (the link is shared with the rest of
+    # this machine's own host->device rate (the link is shared with the rest of
     # the machine, so it varies): copies of the ring's size from the pinned
     # buffer, three before and three after the timed steps
     n_link = min(H, ring.numel())
