@@ -561,6 +561,20 @@ def run_gpu(args):
         "clocks": ck,
         "skip_flags": flags,
     }
+    # A3 on its own: the norm recomputed from the reduced gradients (2 bytes
+    # read per element), as zs_grad_norm does without kept partials
+    torch.cuda.synchronize(dev)
+    n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KN = 5
+    n0.record()
+    for _ in range(KN):         # zs_grad_norm: no loss-scaler state to disturb
+        dw.zs.zs_grad_norm(dw.plan, dw.gs, dw.gP, dw.scratch, True, dw.max_norm, dw.d_norm,
+                           dw.d_coef, dw.d_flags)
+    n1.record()
+    torch.cuda.synchronize(dev)
+    nms = n0.elapsed_time(n1) / KN
+    res["norm_recompute"] = {"ms": nms, "gbs": 2 * dw.info["psi"] / (nms * 1e-3) / 1e9,
+                             "launches": 3, "bytes_per_element": 2}
     # the same step through the per-call API, for comparison (not the value)
     dw.unfused_step()
     torch.cuda.synchronize(dev)

@@ -194,7 +194,15 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
 
 // Recompute the per-tile partial sums from the reduced gradients, with
 // the chunks and the thread mapping of rs_kernel (8-element chunks aligned in
-// the source, chunk gi on thread gi mod THREADS), so the same bits.
+// the source, chunk gi on thread gi mod THREADS, taken in increasing gi), so
+// the same bits.  A thread loads up to four of its chunks before it adds any
+// of them.  A whole chunk whose destination is off a 16-byte boundary is
+// read as the two aligned vectors around it and shifted: shard rows and
+// persistent space start and end on 8-element boundaries, so both vectors
+// lie in the chunk's row (they may cover a neighbouring tile's elements,
+// which are not used).
+constexpr int NORM_BATCH = 4;
+
 template <class T>
 __global__ void __launch_bounds__(THREADS)
 norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__ gs,
@@ -206,25 +214,39 @@ norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__
     const int64_t D = tile.dst, V = tile.valid;
     const int64_t delta = tile.src - D;
     const int64_t vs = tile.src, ve = tile.src + V;
-    const int a = (int)((-delta) & 7);
     const int64_t c_first = vs >> 3;
     const int64_t nchunks = V > 0 ? ((ve - 1) >> 3) - c_first + 1 : 0;
     float sq32 = 0.0f;
     double sq64 = 0.0;
-    for (int64_t gi = threadIdx.x; gi < nchunks; gi += THREADS) {
-        const int64_t c = c_first + gi;
-        const int64_t lo = vs - 8 * c, hi = ve - 8 * c;
-        const int64_t y0 = 8 * c - delta;
-        uint32_t r[8];
-        if (a == 0 && lo <= 0 && hi >= 8) {
-            const uint4 v = ldg16(in + y0);
+    for (int64_t g0 = threadIdx.x; g0 < nchunks; g0 += NORM_BATCH * THREADS) {
+        uint4 v[NORM_BATCH];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) r[i] = lane16(v, i);
-        } else {
+        for (int u = 0; u < NORM_BATCH; ++u) {
+            const int64_t gi = g0 + (int64_t)u * THREADS;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (gi >= nchunks) continue;
+            const int64_t c = c_first + gi;
+            const int64_t lo = vs - 8 * c, hi = ve - 8 * c;
+            const int64_t y0 = 8 * c - delta;
+            if (lo <= 0 && hi >= 8) {
+                const int q = (int)(y0 & 7);
+                v[u] = ldg16(in + (y0 - q));
+                if (q) v[u] = shift8(v[u], ldg16(in + (y0 - q) + 8), q);
+            } else {
+                uint32_t r[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) r[i] = (i >= lo && i < hi) ? (uint32_t)in[y0 + i] : 0u;
+                for (int i = 0; i < 8; ++i) r[i] = (i >= lo && i < hi) ? (uint32_t)in[y0 + i] : 0u;
+                v[u] = pack8(r);
+            }
         }
-        group_sq<T>(r, sq32, sq64);
+#pragma unroll
+        for (int u = 0; u < NORM_BATCH; ++u) {
+            if (g0 + (int64_t)u * THREADS >= nchunks) continue;
+            uint32_t r[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r[i] = lane16(v[u], i);
+            group_sq<T>(r, sq32, sq64);
+        }
     }
     const double s = block_sum(__dadd_rn((double)sq32, sq64), red);
     if (threadIdx.x == 0) partials[t] = s;
