@@ -312,3 +312,23 @@ def test_argument_errors_enqueue_nothing():
     after = d.snapshot()
     for k in before:
         assert np.array_equal(before[k].view(np.uint8), after[k].view(np.uint8))
+
+
+@pytest.mark.parametrize("case", ["ragged_n16_chunks", "many_small_64", "n256_max_ranks"])
+def test_same_steps_twice_same_bits(case):
+    """Determinism: the fused step run twice from the same start on the same
+    gradients gives the same bits everywhere (the rank sum and the norm tree
+    are fixed; no atomics decide an order)."""
+    runs = []
+    for _ in range(2):
+        d = make(case)
+        d.init_weights()
+        for t in (1, 2):
+            d.set_grads(900 + t, use_gpu_generator=(case == "many_small_64"))
+            d.shard_step(HP, t, 1.0)
+        runs.append((d.snapshot(), d.flat.u16().copy(), float(d.d_norm.np()[0])))
+        d.check_canaries()
+    (sa, fa, na), (sb, fb, nb) = runs
+    for k in sa:
+        assert np.array_equal(sa[k].view(np.uint8), sb[k].view(np.uint8)), k
+    assert np.array_equal(fa, fb) and na == nb
