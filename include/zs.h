@@ -28,6 +28,9 @@
  * - Device buffers read or written with 16-byte vectors must be 16-byte
  *   aligned: every buffer except the flat output of the gathers, which needs
  *   only 2-byte alignment.  Misalignment is ZS_EINVAL.
+ * - Host threads: a plan is read-only once uploaded (zs_plan_upload), so
+ *   calls on one plan may come from several threads; a scheduler (zs_sched)
+ *   holds mutable state and must be used by one thread at a time.
  * - Distinct buffers of a call must not overlap (rank gradients, gradient
  *   shards, parameter shards, each state buffer, the persistent buffers, the
  *   flat output, scratch); a buffer the call updates in place (the fp32

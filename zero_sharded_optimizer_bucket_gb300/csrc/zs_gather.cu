@@ -11,6 +11,8 @@
 // one 16-byte load (two and a lane shift when the phases differ) and one
 // 16-byte store.  Slots that straddle a shard boundary are assembled one by
 // one.
+#include <atomic>
+
 #include "zs_device.cuh"
 #include "zs_launch.h"
 
@@ -276,12 +278,13 @@ cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *
         // per device: the kernel's shared-memory opt-in, and the default
         // grid of 8 CTAs per SM: CTAs queue behind the resident ones, which
         // measured faster than one wave of resident CTAs
-        static int wave_of[64] = {};
+        // (atomic: host threads may launch gathers at once; both set it the same)
+        static std::atomic<int> wave_of[64];
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        int wave = wave_of[dev];
+        int wave = wave_of[dev].load(std::memory_order_relaxed);
         if (wave <= 0) {
             int sms = 0;
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -290,7 +293,8 @@ cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          BULK_SMEM_ALLOC);
             if (e != cudaSuccess) return e;
-            wave = wave_of[dev] = 8 * (sms > 0 ? sms : 152);
+            wave = 8 * (sms > 0 ? sms : 152);
+            wave_of[dev].store(wave, std::memory_order_relaxed);
         }
         const int64_t chunks = (a.out_hi - a.out_lo + BULK_CHUNK_ELEMS - 1) / BULK_CHUNK_ELEMS;
         const int64_t cap = max_ctas > 0 ? max_ctas : wave;
