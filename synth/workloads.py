@@ -185,6 +185,15 @@ def llama3_8b_hsdp() -> Workload:
     return w
 
 
+def many_small_prof() -> Workload:
+    """200 parameters drawn like many_small (log-uniform sizes, N=64): the
+    small case for detailed profiles of that list (2.5 GB of rank gradients
+    per step, twenty times the L2)."""
+    w = many_small(200)
+    w.name, w.steps = "many_small_prof", 1
+    return w
+
+
 def giant_param() -> Workload:
     """One parameter of 2^31 + 5 elements (past any 32-bit element index)
     beside two small ones, N=2: an edge case of the kernels' index
@@ -205,6 +214,7 @@ WORKLOADS = {
     "llama3_8b_fp16": llama3_8b_fp16,
     "llama3_8b_hsdp": llama3_8b_hsdp,
     "giant_param": giant_param,
+    "many_small_prof": many_small_prof,
 }
 
 
