@@ -28,6 +28,11 @@
  * - Device buffers read or written with 16-byte vectors must be 16-byte
  *   aligned: every buffer except the flat output of the gathers, which needs
  *   only 2-byte alignment.  Misalignment is ZS_EINVAL.
+ * - CUDA graphs: the device calls only enqueue work on the given stream
+ *   (no host synchronisation, no allocation), so a sequence of them can be
+ *   captured and replayed; scalars such as the Adam step count and the
+ *   hyper-parameters are captured by value (re-capture, or update the
+ *   kernel nodes, to advance them).
  * - Host threads: a plan is read-only once uploaded (zs_plan_upload), so
  *   calls on one plan may come from several threads; a scheduler (zs_sched)
  *   holds mutable state and must be used by one thread at a time.
