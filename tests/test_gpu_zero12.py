@@ -27,10 +27,16 @@ pytestmark = pytest.mark.gpu
 HP = P.HP
 
 
-@pytest.mark.parametrize("case", ["tiny_thr100", "ragged_n16_chunks", "many_small_64"])
+@pytest.mark.parametrize("case", ["tiny_thr100", "ragged_n16_chunks", "many_small_64",
+                                  "ragged_n16_chunks_hsdp4"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_zero2_step_equals_zero3_replica(case, dtype):
-    kw = dict(P.CASES[case], dtype=dtype, log2_scale=-2)
+    """The last case is HSDP (groups of 4 of the 16 ranks): stage-2
+    residency within each replica group."""
+    if case.endswith("_hsdp4"):
+        kw = dict(P.CASES[case[:-len("_hsdp4")]], dtype=dtype, log2_scale=-2, group=4)
+    else:
+        kw = dict(P.CASES[case], dtype=dtype, log2_scale=-2)
     a, b = H.DevicePlan(**kw), H.DevicePlan(**kw)
     for d in (a, b):
         d.init_weights()
