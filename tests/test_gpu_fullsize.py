@@ -185,3 +185,65 @@ def test_fullsize_sampled(name):
         del dw
         gc.collect()
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "many_small", "llama3_8b_fp16", "llama3_8b_hsdp"])
+def test_fullsize_whole_buckets(name):
+    """Every element of whole reduce buckets at full size (the first two,
+    the middle one, the last one and every 64th): reduced gradient bit for
+    bit, fp32 master / moments within tolerance, the cast parameter within
+    one ulp, and its place in the gathered replica.  The rank gradients are
+    read back from the device pool the shared generator filled (its GPU fill
+    is pinned bit for bit to the CPU one), not regenerated on the host."""
+    w = workloads.WORKLOADS[name]()
+    op = _oracle_plan(w)
+    dw = bench.DeviceWorkload(w, "cuda:0", max_norm=0.0)
+    try:
+        dw.step()
+        torch.cuda.synchronize()
+        N, S = op.n_ranks, op.S
+        # max_norm = 0: no clipping; the coefficient is 1 / loss scale
+        coef = np.float32(1.0) / np.float32(w.loss_scale if w.dtype == "fp16" else 1.0)
+        within_ulp = H.assert_fp16_within_ulp if w.dtype == "fp16" else H.assert_bf16_within_ulp
+        c = ostep.adam_consts(w.hparams(), 1)
+        nb = len(op.reduce_buckets)
+        picks = sorted({0, min(1, nb - 1), nb // 2, nb - 1, *range(0, nb, 64)})
+        checked = 0
+        for b in picks:
+            for ent in op.reduce_buckets[b]:
+                p = op.params[ent.param]
+                L = ent.e_hi - ent.e_lo
+                e = np.arange(ent.e_lo, ent.e_hi, dtype=np.int64)
+                rows = [dw.pool[dw.offs[b][k] + ent.buf_off:dw.offs[b][k] + ent.buf_off + L]
+                        for k in range(N)]
+                vals = torch.stack(rows).cpu().numpy().view(np.uint16)
+                gs_ref = ostep.reduce_mean_groups(vals, op.group, w.dtype)
+                if p.persistent:
+                    idx = torch.from_numpy(p.persist_off + e).to(dw.dev)
+                    got_g = dw.gP.index_select(0, idx)
+                    got_p, got_ps = dw.pm.index_select(0, idx), dw.pP.index_select(0, idx)
+                    got_m, got_v = dw.pmm.index_select(0, idx), dw.pmv.index_select(0, idx)
+                else:
+                    r, j = e // p.ps, e % p.ps
+                    idx = torch.from_numpy(r * S + p.shard_off + j).to(dw.dev)
+                    got_g = dw.gs.index_select(0, idx)
+                    got_p, got_ps = dw.master.index_select(0, idx), dw.ps.index_select(0, idx)
+                    got_m, got_v = dw.m.index_select(0, idx), dw.v.index_select(0, idx)
+                assert np.array_equal(got_g.cpu().numpy().view(np.uint16), gs_ref), (b, p.index)
+                W = philox.weight_f32(w.seed, (p.input_off + e).astype(np.uint64), w.weight_sigma)
+                z = np.zeros_like(W)
+                p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, coef, c, w.dtype)
+                H.assert_f32_close(got_p.cpu().numpy(), p1, "master")
+                H.assert_f32_close(got_m.cpu().numpy(), m1, "exp_avg")
+                H.assert_f32_close(got_v.cpu().numpy(), v1, "exp_avg_sq")
+                pbits = got_ps.cpu().numpy().view(np.uint16)
+                within_ulp(pbits, pb, "params")
+                if not p.persistent:
+                    fl = dw.flat.index_select(0, torch.from_numpy(p.flat_off + e).to(dw.dev))
+                    assert np.array_equal(fl.cpu().numpy().view(np.uint16), pbits)
+                checked += L
+        assert checked > 0
+    finally:
+        del dw
+        gc.collect()
+        torch.cuda.empty_cache()
