@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass
+from fractions import Fraction
 
 import numpy as np
 
@@ -189,6 +190,12 @@ def unscale_and_clip(plan: Plan, st: State, max_norm: float, scale: float):
         total = math.fsum(sq.tolist())
     else:
         total = float(np.sum(sq))
+    return clip_from_sumsq(total, max_norm, scale)
+
+
+def clip_from_sumsq(total: float, max_norm: float, scale: float = 1.0):
+    """The finish of unscale_and_clip from the sum of squares of the stored
+    gradients (float64): (norm, coef, skip) as documented there."""
     S = F32(scale)
     norm = F32(np.sqrt(np.float64(total))) / S
     skip = not bool(np.isfinite(norm))
@@ -199,6 +206,66 @@ def unscale_and_clip(plan: Plan, st: State, max_norm: float, scale: float):
         c = F32(max_norm) / (norm + CLIP_EPS)
         clip = c if c < F32(1.0) else F32(1.0)
     return norm, clip / S, False
+
+
+# ------------------------------------------------ A3, bucket by bucket ---
+# The global norm of a model too large to hold the oracle's whole state:
+# the reduced gradients are formed one reduce bucket at a time, as the pages'
+# backward pass produces them ([ZeRO-3 chapter] §6.2, IPG bucket), and only
+# the multiset of their values is kept: how many times each 16-bit |x| bit
+# pattern occurs.  The sum of squares is then sum over patterns of
+# count * value^2, evaluated exactly in rationals and rounded once, which is
+# the same correctly rounded float64 as the fsum of unscale_and_clip.
+def bucket_sq_counts(plan: Plan, bucket: int, rank_bufs) -> np.ndarray:
+    """Occurrences (int64, 2^15 bins indexed by the bits of |x|) of the
+    reduced gradient values that reduce_scatter writes for bucket `bucket`:
+    each element of each of the bucket's entries once, the rank mean taken
+    as reduce_scatter takes it (reduce_mean_groups).  Padding elements are
+    zero and left out.  rank_bufs[k] is rank k's gradient buffer of the
+    bucket."""
+    counts = np.zeros(1 << 15, dtype=np.int64)
+    assert len(rank_bufs) == plan.n_ranks
+    for ent in plan.reduce_buckets[bucket]:
+        L = ent.e_hi - ent.e_lo
+        if L <= 0:
+            continue
+        vals = np.stack([np.asarray(b[ent.buf_off:ent.buf_off + L]) for b in rank_bufs])
+        red = reduce_mean_groups(vals, plan.group, plan.dtype)
+        counts += np.bincount(red & np.uint16(0x7FFF), minlength=1 << 15)
+    return counts
+
+
+def sumsq_from_counts(counts, dtype: str = "bf16") -> float:
+    """sum over bit patterns of count * value^2, exact (Fraction), rounded
+    once to float64; inf when an infinite value occurs, nan when a NaN
+    does."""
+    counts = np.asarray(counts, dtype=np.int64)
+    nz = np.nonzero(counts)[0]
+    vals = to_f32(nz.astype(np.uint16), dtype)
+    if np.any(np.isnan(vals)):
+        return float("nan")
+    if np.any(np.isinf(vals)):
+        return float("inf")
+    total = Fraction(0)
+    for c, v in zip(counts[nz].tolist(), vals.tolist()):
+        total += c * Fraction(v) ** 2
+    return float(total)
+
+
+def grad_norm_streamed(plan: Plan, bucket_bufs, max_norm: float, scale: float = 1.0):
+    """unscale_and_clip computed bucket by bucket: bucket_bufs yields
+    (bucket, rank_bufs) for every reduce bucket once, in any order (the
+    counts add up).  Returns (norm, coef, skip)."""
+    counts = np.zeros(1 << 15, dtype=np.int64)
+    seen = set()
+    for b, rank_bufs in bucket_bufs:
+        if b in seen:
+            raise ValueError(f"bucket {b} given twice")
+        seen.add(b)
+        counts += bucket_sq_counts(plan, b, rank_bufs)
+    if len(seen) != len(plan.reduce_buckets):
+        raise ValueError("every reduce bucket must be given once")
+    return clip_from_sumsq(sumsq_from_counts(counts, plan.dtype), max_norm, scale)
 
 
 @dataclass

@@ -101,6 +101,26 @@ def _unscale_forgets_scale(plan, st, max_norm, scale):
     return norm, (coef * np.float32(scale) if not skip else coef), skip
 
 
+_orig_counts = ostep.bucket_sq_counts
+
+
+def _counts_skip_persistent(plan, bucket, rank_bufs):
+    kept = [e for e in plan.reduce_buckets[bucket] if not plan.params[e.param].persistent]
+    import dataclasses
+    plan2 = dataclasses.replace(plan, reduce_buckets=[
+        kept if b == bucket else ents for b, ents in enumerate(plan.reduce_buckets)])
+    return _orig_counts(plan2, bucket, rank_bufs)
+
+
+def _sumsq_float32(counts, dtype="bf16"):
+    counts = np.asarray(counts)
+    vals = ostep.to_f32(np.arange(1 << 15, dtype=np.uint16), dtype)
+    tot = np.float32(0)
+    for i in np.nonzero(counts)[0]:
+        tot = tot + np.float32(counts[i]) * vals[i] * vals[i]
+    return float(tot)
+
+
 class _GreedyScaler(ostep.LossScaler):
     def update(self, overflow):
         if overflow:
@@ -141,6 +161,10 @@ MUTANTS = [
      _fp16_pin_unscale),
     ("loss scale grows every good step", ostep, "LossScaler", _GreedyScaler,
      _fp16_pin_schedule),
+    ("streamed norm leaves out persistent parameters", ostep, "bucket_sq_counts",
+     _counts_skip_persistent, lambda: pins.test_streamed_norm_equals_whole_state_norm("tiny_thr100")),
+    ("streamed sum of squares in float32", ostep, "sumsq_from_counts", _sumsq_float32,
+     pins.test_sumsq_from_counts_is_exact),
 ]
 
 

@@ -412,6 +412,104 @@ def test_norm_nonfinite_sets_skip():
     assert np.array_equal(before, st.master)
 
 
+# ------------------------------------------------ norm, streamed ---------
+def _streamed(plan, bufs, max_norm, scale=1.0, order=None):
+    order = range(len(bufs)) if order is None else order
+    return ostep.grad_norm_streamed(plan, ((b, bufs[b]) for b in order), max_norm, scale)
+
+
+def test_streamed_norm_worked_example():
+    """[Grok blog] 具体例子: identical full gradients [0.5, 1, 1.5, 2] on the
+    4 GPUs; the global norm of their mean is sqrt(7.5)."""
+    ex = golden("worked_example.json")
+    N = ex["n_ranks"]
+    plan = oplan.build_partition([len(ex["weights"])], N, threshold=0)
+    g = f32_to_bf16(np.array(ex["full_grads_every_rank"], dtype=np.float32))
+    bufs = helpers.bucket_buffers(plan, [g] * N)
+    norm, coef, skip = _streamed(plan, bufs, 1.0)
+    assert not skip
+    assert float(norm) == float(np.float32(math.sqrt(7.5)))
+    assert abs(float(coef) - 1.0 / (math.sqrt(7.5) + 1e-6)) <= 1e-6
+
+
+def test_streamed_norm_equals_unsharded_norm():
+    """Bucket by bucket, the norm is that of the unpartitioned all-reduce
+    mean (numpy.linalg.norm), for any order of the buckets."""
+    plan, st, full_mean, G, bufs = _setup_random(seed=6)
+    ref = np.linalg.norm(np.concatenate(full_mean).astype(np.float64))
+    rng = np.random.default_rng(1)
+    for order in (None, list(rng.permutation(len(bufs)))):
+        norm, coef, skip = _streamed(plan, bufs, 1.0, order=order)
+        assert not skip
+        assert abs(float(norm) - ref) <= 1e-7 * ref
+
+
+@pytest.mark.parametrize("kind", ["tiny_thr100", "ragged_chunks", "hsdp", "fp16", "many_small"])
+def test_streamed_norm_equals_whole_state_norm(kind):
+    """The same correctly rounded sum of squares as the norm over the
+    reduce-scattered state: equal bits, clip coefficient included."""
+    from synth import workloads
+    rng = np.random.default_rng(3)
+    dtype, scale, group = "bf16", 1.0, None
+    if kind == "tiny_thr100":
+        numel, N, kw = workloads.tiny().numel, 4, dict(threshold=100)
+    elif kind == "ragged_chunks":
+        numel = [int(x) for x in rng.integers(0, 3000, size=25)] + [2501, 1]
+        N, kw = 7, dict(threshold=50, reduce_bucket_size=333)
+    elif kind == "hsdp":
+        numel = [int(x) for x in rng.integers(0, 3000, size=25)]
+        N, kw, group = 12, dict(threshold=50, reduce_bucket_size=900), 3
+    elif kind == "fp16":
+        numel = [int(x) for x in rng.integers(0, 3000, size=25)]
+        N, kw, dtype, scale = 16, dict(threshold=50, reduce_bucket_size=900), "fp16", 1024.0
+    else:
+        # the smaller tensors of the many-small list at N = 64: heavy padding
+        numel = [x for x in workloads.many_small(200).numel if x < 20_000][:20]
+        N, kw = 64, dict(threshold=2000, reduce_bucket_size=30_000)
+    plan = oplan.build_partition(numel, N, dtype=dtype, shard_group_size=group, **kw)
+    n = plan.input_elems
+    if dtype == "fp16":
+        G = [philox.grad_fp16(5, 0, np.arange(k * n, (k + 1) * n, dtype=np.uint64), -3)
+             for k in range(N)]
+    else:
+        G = helpers.full_grads_from_pool(plan, 5, 1e-2, N, outlier_frac=0.01)
+    bufs = helpers.bucket_buffers(plan, G)
+    st = ostep.new_state(plan)
+    for b in range(len(plan.reduce_buckets)):
+        ostep.reduce_scatter(plan, b, bufs[b], st)
+    for max_norm in (1.0, 0.0):
+        a = ostep.unscale_and_clip(plan, st, max_norm, scale)
+        b = _streamed(plan, bufs, max_norm, scale, order=list(rng.permutation(len(bufs))))
+        assert a[2] == b[2] is False
+        assert np.float32(a[0]).tobytes() == np.float32(b[0]).tobytes()
+        assert np.float32(a[1]).tobytes() == np.float32(b[1]).tobytes()
+
+
+def test_sumsq_from_counts_is_exact():
+    """1 + 2^20 * (2^-30)^2 = 1 + 2^-40 needs 41 bits: exact in float64,
+    lost by a float32 sum."""
+    counts = np.zeros(1 << 15, dtype=np.int64)
+    one = int(f32_to_bf16(np.array([1.0], np.float32))[0])
+    tiny = int(f32_to_bf16(np.array([2.0 ** -30], np.float32))[0])
+    counts[one] = 1
+    counts[tiny] = 1 << 20
+    assert ostep.sumsq_from_counts(counts) == 1.0 + 2.0 ** -40
+    assert ostep.sumsq_from_counts(np.zeros(1 << 15, np.int64)) == 0.0
+
+
+def test_streamed_norm_nonfinite_and_every_bucket_once():
+    plan, st, full_mean, G, bufs = _setup_random(seed=8)
+    bad = [[b.copy() for b in row] for row in bufs]
+    e = plan.reduce_buckets[1][0]
+    bad[1][2][e.buf_off] = 0x7F80          # +inf in rank 2's gradient
+    norm, coef, skip = _streamed(plan, bad, 1.0)
+    assert skip and coef == 1.0
+    with pytest.raises(ValueError):
+        _streamed(plan, bufs, 1.0, order=[0] + list(range(len(bufs))))
+    with pytest.raises(ValueError):
+        _streamed(plan, bufs, 1.0, order=list(range(1, len(bufs))))
+
+
 # ------------------------------------------------------------- adam ------
 @pytest.mark.parametrize("adamw", [1, 0])
 def test_adam_matches_torch(adamw):
