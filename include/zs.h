@@ -292,10 +292,17 @@ zs_status zs_reduce_scatter(const zs_plan *plan, int32_t bucket, const void *con
  * norm must cover all shards, each rank alone would clip differently).
  * norm = sqrt(sum of squares of every shard element and every persistent
  * element); coef = min(1, max_norm / (norm + 1e-6)) in fp32, 1 when
- * max_norm <= 0 or when the norm is not finite.  recompute = 0 uses the
- * per-tile sums that zs_reduce_scatter left in norm_scratch (every bucket
- * must have been reduced with it since); recompute = 1 first recomputes
- * them from grad_shards / persist_grads.  Writes device scalars d_norm,
+ * max_norm <= 0 or when the norm is not finite.  The sum of squares is
+ * accumulated without rounding error up to about 2^-46 relative (squares
+ * of 16-bit values are exact in fp32, each addition's error is carried in
+ * a float32 pair, the per-tile sums and above are float64), then
+ * norm = float32(sqrt(sum)) as with an exactly rounded sum, so the norm
+ * and the coefficient have the bits of the exact definition except when
+ * the root lies within that error of a float32 rounding boundary.
+ * recompute = 0 uses the per-tile sums that zs_reduce_scatter left in
+ * norm_scratch (every bucket must have been reduced with it since);
+ * recompute = 1 first recomputes them from grad_shards / persist_grads,
+ * with the same bits.  Writes device scalars d_norm,
  * d_clip_coef and the flag word d_flags (ZS_SKIP_NONFINITE).  Errors:
  * ZS_EINVAL, ZS_ESTATE, ZS_ECUDA. */
 zs_status zs_grad_norm(const zs_plan *plan, const void *grad_shards, const void *persist_grads,
@@ -353,7 +360,10 @@ zs_status zs_unscale_and_clip(const zs_plan *plan, const void *grad_shards,
  * bit.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept per device and per
+ *   CUDA context: after the device's context is destroyed and created again
+ *   (cudaDeviceReset), the next call looks it up again, so that call too
+ *   should come before any capture.
  * - Every call on a device shares the one array and it keeps the last
  *   call's contents; each call writes every element it reads, so nothing
  *   needs clearing.  Calls that overlap on the GPU (other streams, other

@@ -9,8 +9,14 @@
 //
 // The array is ZS_NOALLOC_NORM_MAX_SCRATCH doubles (8 MiB) in device memory,
 // held by every GPU that loads the library until the process exits.  Its
-// address is looked up once per device (cudaGetSymbolAddress, with that
-// device current) on the first call made on that device.
+// address is looked up (cudaGetSymbolAddress, with that device current) on
+// the first call made on a device, and again on the first call after the
+// device's context was destroyed and created anew (cudaDeviceReset), when
+// the module holding the array is loaded again, possibly elsewhere.  The
+// cache is keyed on the context's process-unique id (cuCtxGetId), which a
+// new context never shares with an old one.
+#include <cuda.h>
+
 #include <cstdint>
 #include <mutex>
 
@@ -22,10 +28,40 @@ namespace {
 
 constexpr int kMaxDevices = 256;
 std::mutex g_mu;
-double *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_norm_scratch on the current device.  The name of the
-// array in host code is only a host-side stand-in, never a device address.
+struct DeviceScratch {
+    unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+    double *addr;
+};
+DeviceScratch g_scratch[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// The driver's context queries, through the runtime (no link-time
+// dependency on the driver library).  Called with g_mu held.
+zs_status resolve_driver_entry_points() {
+    if (g_ctx_get_current && g_ctx_get_id) return ZS_OK;
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+    void *f1 = nullptr, *f2 = nullptr;
+    const cudaError_t e1 =
+        cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
+    const cudaError_t e2 =
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || q1 != cudaDriverEntryPointSuccess ||
+        q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+        return zs_fail(ZS_ECUDA, "zs_grad_norm_noalloc: driver context queries unavailable (%s)",
+                       cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    return ZS_OK;
+}
+
+// Device address of g_norm_scratch in the current device's current context.
+// The name of the array in host code is only a host-side stand-in, never a
+// device address.
 zs_status scratch_address(double **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -34,15 +70,31 @@ zs_status scratch_address(double **out) {
     if (dev < 0 || dev >= kMaxDevices)
         return zs_fail(ZS_EINVAL, "zs_grad_norm_noalloc: device %d out of range", dev);
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    zs_status r = resolve_driver_entry_points();
+    if (r) return r;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+        // no context current on this thread yet: make the device's primary
+        // context current (cudaSetDevice initialises it; nothing is allocated)
+        e = cudaSetDevice(dev);
+        if (e != cudaSuccess || g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx)
+            return zs_fail(ZS_ECUDA, "zs_grad_norm_noalloc: no CUDA context on device %d (%s)",
+                           dev, cudaGetErrorString(e));
+    }
+    unsigned long long id = 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS || id == 0)
+        return zs_fail(ZS_ECUDA, "zs_grad_norm_noalloc: cuCtxGetId failed on device %d", dev);
+    DeviceScratch &ds = g_scratch[dev];
+    if (ds.ctx_id != id || !ds.addr) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_norm_scratch);
         if (e != cudaSuccess || !p)
             return zs_fail(ZS_ECUDA, "zs_grad_norm_noalloc: cudaGetSymbolAddress: %s",
                            cudaGetErrorString(e));
-        g_scratch_addr[dev] = static_cast<double *>(p);
+        ds.addr = static_cast<double *>(p);
+        ds.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = ds.addr;
     return ZS_OK;
 }
 

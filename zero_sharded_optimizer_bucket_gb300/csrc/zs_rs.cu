@@ -25,7 +25,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
           const uint16_t *const *__restrict__ table, int N, int G, float fN,
           uint16_t *__restrict__ gs, uint16_t *__restrict__ gP, double *__restrict__ partials) {
     __shared__ const uint16_t *sp[ZS_MAX_RANKS];
-    __shared__ double red[WARPS];
+    __shared__ SqRed red;
     __shared__ int bad;
     // Launched as a programmatic dependent: wait until the previous kernel
     // of the stream has finished and its writes are visible (a no-op in an
@@ -68,8 +68,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     // far cheaper than an IEEE division.  Other N divide.
     const bool pow2 = (N & (N - 1)) == 0;
     const float invN = 1.0f / fN;
-    float sq32 = 0.0f;
-    double sq64 = 0.0;
+    SqAcc sq;
     // uniform trip count: every lane takes part in the shuffles
     for (int64_t base = 0; base < nchunks; base += THREADS) {
         const int64_t gi = base + threadIdx.x;
@@ -140,7 +139,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             r[i] = act ? T::from_f32(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN)) : 0u;
-        if (act) group_sq<T>(r, sq32, sq64);
+        if (act) group_sq<T>(r, sq);
         const int64_t y0 = 8 * c - delta;  // destination of lane 0 of the chunk
         if (a == 0) {
             if (act) {
@@ -187,7 +186,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         }
     }
     if (partials) {
-        const double s = block_sum(__dadd_rn((double)sq32, sq64), red);
+        const double s = block_sum_sq(sq, red);
         if (threadIdx.x == 0) partials[t] = s;
     }
 }
@@ -207,7 +206,7 @@ template <class T>
 __global__ void __launch_bounds__(THREADS)
 norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__ gs,
                   const uint16_t *__restrict__ gP, double *__restrict__ partials) {
-    __shared__ double red[WARPS];
+    __shared__ SqRed red;
     const int64_t t = blockIdx.x;
     const ZsTile tile = tiles[t];
     const uint16_t *__restrict__ in = tile.flat < 0 ? gP : gs;
@@ -216,8 +215,7 @@ norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__
     const int64_t vs = tile.src, ve = tile.src + V;
     const int64_t c_first = vs >> 3;
     const int64_t nchunks = V > 0 ? ((ve - 1) >> 3) - c_first + 1 : 0;
-    float sq32 = 0.0f;
-    double sq64 = 0.0;
+    SqAcc sq;
     for (int64_t g0 = threadIdx.x; g0 < nchunks; g0 += NORM_BATCH * THREADS) {
         uint4 v[NORM_BATCH];
 #pragma unroll
@@ -245,10 +243,10 @@ norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__
             uint32_t r[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) r[i] = lane16(v[u], i);
-            group_sq<T>(r, sq32, sq64);
+            group_sq<T>(r, sq);
         }
     }
-    const double s = block_sum(__dadd_rn((double)sq32, sq64), red);
+    const double s = block_sum_sq(sq, red);
     if (threadIdx.x == 0) partials[t] = s;
 }
 
