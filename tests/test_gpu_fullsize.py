@@ -1,17 +1,26 @@
-"""Full-size parity on sampled outputs, in the launch configuration bench.py
-times (bench.DeviceWorkload + zs_shard_step).
+"""Full-size parity, in the launch configuration bench.py times
+(bench.DeviceWorkload + zs_shard_step).
 
-The oracle computes each sampled element on its own: the N rank gradients
-of that element (drawn by synth at the element's pool position), the rank
-mean, one AdamW step from the partitioned initial weight.  max_norm = 0
-makes the clip coefficient exactly 1 on both sides, so no value computed by
-the device is ever an input of the oracle.  The gradient norm at full size
-is checked through a property that holds at any size: it equals the norm
-of the device's reduced-gradient buffers (float64 sum).
+test_fullsize_sampled: max_norm = 0 makes the clip coefficient exactly
+1 / loss scale on both sides, so the device's state must equal the oracle's
+bit for bit.  The oracle computes each sampled element on its own: the N
+rank gradients of that element (drawn by synth at the element's pool
+position), the rank mean, one AdamW step from the partitioned initial
+weight.
+
+test_fullsize_whole_buckets: the workloads' own settings, clipping on
+(max_norm 1.0) and their step counts (5 AdamW steps for the many-small
+list).  The oracle's global norm is streamed over every reduce bucket
+(oracle.step.bucket_sq_counts on the N rank buffers of each bucket, read
+back from the device pool the shared generator filled); its clip
+coefficient drives the oracle's Adam on whole buckets.  No value the
+device computes is an input of the oracle.
 """
 from __future__ import annotations
 
 import gc
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -119,13 +128,12 @@ def test_fullsize_sampled(name):
         p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, coef,
                                            ostep.adam_consts(w.hparams(), 1), w.dtype)
         assert np.array_equal(got["gs"].view(np.uint16)[data], gs_ref)
-        H.assert_f32_close(got["p"][data], p1, "master")
-        H.assert_f32_close(got["m"][data], m1, "exp_avg")
-        H.assert_f32_close(got["v"][data], v1, "exp_avg_sq")
-        if w.dtype == "fp16":
-            H.assert_fp16_within_ulp(got["ps"].view(np.uint16)[data], pb, "param_shards")
-        else:
-            H.assert_bf16_within_ulp(got["ps"].view(np.uint16)[data], pb, "param_shards")
+        # the same coefficient bits on both sides: the same float32 operations
+        H.assert_state({"master": got["p"][data], "exp_avg": got["m"][data],
+                        "exp_avg_sq": got["v"][data]},
+                       {"master": p1, "exp_avg": m1, "exp_avg_sq": v1}, None,
+                       f"{name} sampled", True, keys=("master", "exp_avg", "exp_avg_sq"))
+        H.assert_16bit(got["ps"].view(np.uint16)[data], pb, "param_shards", w.dtype, True)
         # padding and alignment columns stay exactly zero
         for k in ("gs", "ps", "p", "m", "v"):
             assert not np.any(got[k].view(np.uint8).reshape(len(cols), -1)[~data])
@@ -172,7 +180,8 @@ def test_fullsize_sampled(name):
             zp = np.zeros_like(Wp)
             pp1 = ostep.adam_update(Wp, zp, zp, gP_ref, coef,
                                     ostep.adam_consts(w.hparams(), 1), w.dtype)[0]
-            H.assert_f32_close(dw.pm.index_select(0, pidx2).cpu().numpy(), pp1, "p_master")
+            got_pm = dw.pm.index_select(0, pidx2).cpu().numpy()
+            assert np.array_equal(got_pm.view(np.uint32), pp1.view(np.uint32)), "p_master"
         # the norm is the norm of the reduced-gradient buffers
         tot = 0.0
         for buf, n in ((dw.gs, op.group * op.S), (dw.gP, op.Pn_alloc)):
@@ -187,61 +196,111 @@ def test_fullsize_sampled(name):
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["llama3_8b", "many_small", "llama3_8b_fp16", "llama3_8b_hsdp"])
+def _bucket_rows(dw, op, b):
+    """The N rank gradient buffers of bucket b, read back from the device
+    pool (input data: the shared generator filled it)."""
+    L = op.bucket_buf_elems[b]
+    rows = torch.stack([dw.pool[dw.offs[b][k]:dw.offs[b][k] + L] for k in range(op.n_ranks)])
+    return list(rows.cpu().numpy().view(np.uint16))
+
+
+def oracle_norm_streamed(dw, op, max_norm, scale):
+    """The oracle's (norm, coef, skip) over every reduce bucket: the rank
+    buffers are read back one bucket at a time and handed to the oracle's
+    per-bucket counts, several buckets at once on host threads (numpy
+    releases the interpreter lock in its array loops); counts add up in any
+    order."""
+    nb = len(op.reduce_buckets)
+    workers = max(1, min(16, os.cpu_count() or 1))
+    counts = np.zeros(1 << 15, dtype=np.int64)
+    with ThreadPoolExecutor(workers) as ex:
+        pending = []
+        for b in range(nb):
+            pending.append(ex.submit(ostep.bucket_sq_counts, op, b, _bucket_rows(dw, op, b)))
+            if len(pending) >= 2 * workers:
+                counts += pending.pop(0).result()
+        for f in pending:
+            counts += f.result()
+    return ostep.clip_from_sumsq(ostep.sumsq_from_counts(counts, op.dtype), max_norm, scale)
+
+
+@pytest.mark.parametrize("name", ["llama_layer", "many_small", "llama3_16_layers", "llama3_8b",
+                                  "llama3_8b_fp16", "llama3_8b_hsdp"])
 def test_fullsize_whole_buckets(name):
     """Every element of whole reduce buckets at full size (the first two,
-    the middle one, the last one and every 64th): reduced gradient bit for
-    bit, fp32 master / moments within tolerance, the cast parameter within
-    one ulp, and its place in the gathered replica.  The rank gradients are
-    read back from the device pool the shared generator filled (its GPU fill
-    is pinned bit for bit to the CPU one), not regenerated on the host."""
+    the middle one, the last one and every 64th), with the workload's
+    clipping and step count: the norm against the oracle's streamed norm,
+    the reduced gradient bit for bit, the fp32 master / moments and the cast
+    parameter against the oracle's Adam with the oracle's coefficient (bit
+    for bit when the device's coefficient has the same bits, as the device
+    norm is accumulated without rounding error), and the parameter's place
+    in the gathered replica."""
     w = workloads.WORKLOADS[name]()
     op = _oracle_plan(w)
-    dw = bench.DeviceWorkload(w, "cuda:0", max_norm=0.0)
+    dw = bench.DeviceWorkload(w, "cuda:0", max_norm=w.max_norm)
     try:
-        dw.step()
-        torch.cuda.synchronize()
+        assert w.max_norm > 0
         N, S = op.n_ranks, op.S
-        # max_norm = 0: no clipping; the coefficient is 1 / loss scale
-        coef = np.float32(1.0) / np.float32(w.loss_scale if w.dtype == "fp16" else 1.0)
-        within_ulp = H.assert_fp16_within_ulp if w.dtype == "fp16" else H.assert_bf16_within_ulp
-        c = ostep.adam_consts(w.hparams(), 1)
+        scale = float(w.loss_scale) if w.dtype == "fp16" else 1.0
+        onorm, ocoef, oskip = oracle_norm_streamed(dw, op, w.max_norm, scale)
+        assert not oskip and float(ocoef) * scale < 1.0          # clipping is active
         nb = len(op.reduce_buckets)
         picks = sorted({0, min(1, nb - 1), nb // 2, nb - 1, *range(0, nb, 64)})
-        checked = 0
+        # the oracle's side of every picked entry: reduced gradient, initial state
+        ref = []
         for b in picks:
+            rows = _bucket_rows(dw, op, b)
             for ent in op.reduce_buckets[b]:
                 p = op.params[ent.param]
                 L = ent.e_hi - ent.e_lo
                 e = np.arange(ent.e_lo, ent.e_hi, dtype=np.int64)
-                rows = [dw.pool[dw.offs[b][k] + ent.buf_off:dw.offs[b][k] + ent.buf_off + L]
-                        for k in range(N)]
-                vals = torch.stack(rows).cpu().numpy().view(np.uint16)
+                vals = np.stack([r[ent.buf_off:ent.buf_off + L] for r in rows])
                 gs_ref = ostep.reduce_mean_groups(vals, op.group, w.dtype)
-                if p.persistent:
-                    idx = torch.from_numpy(p.persist_off + e).to(dw.dev)
-                    got_g = dw.gP.index_select(0, idx)
-                    got_p, got_ps = dw.pm.index_select(0, idx), dw.pP.index_select(0, idx)
-                    got_m, got_v = dw.pmm.index_select(0, idx), dw.pmv.index_select(0, idx)
-                else:
-                    r, j = e // p.ps, e % p.ps
-                    idx = torch.from_numpy(r * S + p.shard_off + j).to(dw.dev)
-                    got_g = dw.gs.index_select(0, idx)
-                    got_p, got_ps = dw.master.index_select(0, idx), dw.ps.index_select(0, idx)
-                    got_m, got_v = dw.m.index_select(0, idx), dw.v.index_select(0, idx)
-                assert np.array_equal(got_g.cpu().numpy().view(np.uint16), gs_ref), (b, p.index)
                 W = philox.weight_f32(w.seed, (p.input_off + e).astype(np.uint64), w.weight_sigma)
+                if p.persistent:
+                    idx = p.persist_off + e
+                else:
+                    idx = (e // p.ps) * S + p.shard_off + e % p.ps
                 z = np.zeros_like(W)
-                p1, m1, v1, pb = ostep.adam_update(W, z, z, gs_ref, coef, c, w.dtype)
-                H.assert_f32_close(got_p.cpu().numpy(), p1, "master")
-                H.assert_f32_close(got_m.cpu().numpy(), m1, "exp_avg")
-                H.assert_f32_close(got_v.cpu().numpy(), v1, "exp_avg_sq")
-                pbits = got_ps.cpu().numpy().view(np.uint16)
-                within_ulp(pbits, pb, "params")
+                ref.append(dict(b=b, p=p, e=e, idx=torch.from_numpy(idx).to(dw.dev), gs=gs_ref,
+                                st={"master": W, "exp_avg": z, "exp_avg_sq": z.copy()}))
+        steps = w.steps
+        checked = 0
+        for t in range(1, steps + 1):
+            dw.step()
+            torch.cuda.synchronize()
+            assert int(dw.d_flags[0]) == 0
+            dnorm, dcoef = float(dw.d_norm[0]), float(dw.d_coef[0])
+            assert abs(dnorm - float(onorm)) <= 1e-5 * float(onorm), (dnorm, float(onorm))
+            exact = H.same_bits(dcoef, ocoef)
+            print(f"{name} step {t}: norm {dnorm!r} (oracle {float(onorm)!r}), coefficient "
+                  f"{dcoef!r} (oracle {float(ocoef)!r}): bits {'equal' if exact else 'differ'}")
+            c = ostep.adam_consts(w.hparams(), t)
+            for r in ref:
+                p, e = r["p"], r["e"]
+                prev = r["st"]
+                p1, m1, v1, pb = ostep.adam_update(prev["master"], prev["exp_avg"],
+                                                   prev["exp_avg_sq"], r["gs"], ocoef, c, w.dtype)
+                r["st"] = {"master": p1, "exp_avg": m1, "exp_avg_sq": v1}
+                if t < steps and t != 1:
+                    continue             # compared after the first and the last step
+                idx = r["idx"]
+                if p.persistent:
+                    bufs = (dw.gP, dw.pm, dw.pmm, dw.pmv, dw.pP)
+                else:
+                    bufs = (dw.gs, dw.master, dw.m, dw.v, dw.ps)
+                got_g, got_p, got_m, got_v, got_ps = (x.index_select(0, idx).cpu().numpy()
+                                                      for x in bufs)
+                assert np.array_equal(got_g.view(np.uint16), r["gs"]), (r["b"], p.index)
+                H.assert_state({"master": got_p, "exp_avg": got_m, "exp_avg_sq": got_v},
+                               r["st"], prev, f"{name} step {t} bucket {r['b']} param {p.index}",
+                               exact, keys=("master", "exp_avg", "exp_avg_sq"))
+                pbits = got_ps.view(np.uint16)
+                H.assert_16bit(pbits, pb, "params", w.dtype, exact)
                 if not p.persistent:
                     fl = dw.flat.index_select(0, torch.from_numpy(p.flat_off + e).to(dw.dev))
                     assert np.array_equal(fl.cpu().numpy().view(np.uint16), pbits)
-                checked += L
+                checked += len(e)
         assert checked > 0
     finally:
         del dw

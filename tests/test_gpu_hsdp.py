@@ -46,16 +46,15 @@ def test_hsdp_steps_vs_oracle(case):
     for t in (1, 2):
         d.set_grads(300 + t, use_gpu_generator=case.startswith("many"))
         d.shard_step(HP, t, 1.0)
+        prev = H.oracle_state(d.ost)
         norm, coef, skip, flat = ostep.shard_step(d.op, d.ost, d.grad_bufs, HP, t, 1.0)
         s = d.snapshot()
         assert np.array_equal(s["grad_shards"], d.ost.grad_shards)
         assert np.array_equal(s["persist_grads"], d.ost.persist_grads)
         assert abs(float(d.d_norm.np()[0]) - float(norm)) <= 1e-5 * float(norm)
-        for k, ref in [("master", d.ost.master), ("exp_avg", d.ost.exp_avg),
-                       ("exp_avg_sq", d.ost.exp_avg_sq), ("p_master", d.ost.p_master)]:
-            H.assert_f32_close(s[k], ref, f"{k} step {t}")
-        ulp = H.assert_fp16_within_ulp if d.dtype == "fp16" else H.assert_bf16_within_ulp
-        ulp(d.flat.u16(), flat, "gathered")
+        exact = H.same_bits(d.d_coef.np()[0], coef)
+        H.assert_state(s, d.ost, prev, f"{case} step {t}", exact)
+        H.assert_16bit(d.flat.u16(), flat, "gathered", d.dtype, exact)
     d.check_canaries()
 
 

@@ -144,7 +144,6 @@ def test_adam_isolated_bit_exact(case):
         for k, ref in [("master", d.ost.master), ("exp_avg", d.ost.exp_avg),
                        ("exp_avg_sq", d.ost.exp_avg_sq), ("p_master", d.ost.p_master),
                        ("p_exp_avg", d.ost.p_exp_avg), ("p_exp_avg_sq", d.ost.p_exp_avg_sq)]:
-            H.assert_f32_close(s[k], ref, k)
             assert np.array_equal(s[k].view(np.uint32), ref.view(np.uint32)), k
         assert np.array_equal(s["param_shards"], d.ost.param_shards)
         assert np.array_equal(s["persist_params"], d.ost.persist_params)
@@ -220,24 +219,28 @@ def test_fused_equals_unfused(case):
 
 
 def test_multistep_vs_oracle(case):
-    """Whole steps (fused), state carried over, against the oracle's steps."""
+    """Whole steps (fused), state carried over, against the oracle's steps:
+    the norm within 1e-5; the state, the parameters and the gathered replica
+    bit for bit when the clip coefficients agree in bits, else within the
+    per-element bound.  The many-small list runs its 5 steps."""
     d = make(case)
     d.init_weights()
-    steps = 3 if case.startswith("tiny") else 2
+    steps = 3 if case.startswith("tiny") else 5 if case == "many_small_64" else 2
     for t in range(1, steps + 1):
         d.set_grads(2000 + t, use_gpu_generator=(case == "many_small_64"))
         d.shard_step(HP, t, 1.0)
+        prev = H.oracle_state(d.ost)
         norm, coef, skip, flat = ostep.shard_step(d.op, d.ost, d.grad_bufs, HP, t, 1.0)
         s = d.snapshot()
         assert np.array_equal(s["grad_shards"], d.ost.grad_shards)
         assert abs(float(d.d_norm.np()[0]) - float(norm)) <= 1e-5 * float(norm)
-        for k, ref in [("master", d.ost.master), ("exp_avg", d.ost.exp_avg),
-                       ("exp_avg_sq", d.ost.exp_avg_sq), ("p_master", d.ost.p_master),
-                       ("p_exp_avg", d.ost.p_exp_avg), ("p_exp_avg_sq", d.ost.p_exp_avg_sq)]:
-            H.assert_f32_close(s[k], ref, f"{k} step {t}")
-        H.assert_bf16_within_ulp(s["param_shards"], d.ost.param_shards, "param_shards")
-        H.assert_bf16_within_ulp(s["persist_params"], d.ost.persist_params, "persist_params")
-        H.assert_bf16_within_ulp(d.flat.u16(), flat, "gathered")
+        exact = H.same_bits(d.d_coef.np()[0], coef)
+        print(f"{case} step {t}: norm {float(d.d_norm.np()[0])!r} (oracle {float(norm)!r}), "
+              f"coefficient bits {'equal' if exact else 'differ'}")
+        H.assert_state(s, d.ost, prev, f"{case} step {t}", exact)
+        H.assert_16bit(s["param_shards"], d.ost.param_shards, "param_shards", "bf16", exact)
+        H.assert_16bit(s["persist_params"], d.ost.persist_params, "persist_params", "bf16", exact)
+        H.assert_16bit(d.flat.u16(), flat, "gathered", "bf16", exact)
         # the gathered buffer is exactly the device's own shards, repacked
         part = ostep.gather_model(d.op, s["param_shards"])
         assert np.array_equal(d.flat.u16(), part)

@@ -3,8 +3,10 @@ shards the optimizer state, stage 2 also the gradients, both keep the full
 parameters on every rank).
 
 Stage 2: the fused step without a shard buffer writes the new parameters
-only into the full replica (model flat space) — it must equal the ZeRO-3
-step's gathered output bit for bit and leave the same optimizer state.
+only into the full replica (model flat space).  Its replica and optimizer
+state are checked against the oracle's own steps (the replica against the
+oracle's gather of its updated shards), and against the ZeRO-3 step's
+gathered output and state bit for bit.
 Stage 1: the gradient all-reduce is the reduce-scatter followed by the
 all-gather of the reduced gradients; it must equal the oracle's all-reduce
 mean of the full gradients."""
@@ -45,6 +47,7 @@ def test_zero2_step_equals_zero3_replica(case, dtype):
     sa = torch.tensor([256.0, 0, 0, 0], device=a.dev)
     sb = sa.clone()
     ga, gb = torch.zeros(4, dtype=torch.int32, device=a.dev), torch.zeros(4, dtype=torch.int32, device=a.dev)
+    osc = ostep.LossScaler(scale=256.0, window=2) if dtype == "fp16" else None
     for t in (1, 2, 3):
         for d in (a, b):
             d.set_grads(700 + t, use_gpu_generator=case.startswith("many"))
@@ -60,6 +63,17 @@ def test_zero2_step_equals_zero3_replica(case, dtype):
             zs.zs_shard_step(b.plan, b.ptr_table, st2, b.scratch.ptr(), HP, t, 1.0, b.d_norm.ptr(),
                              b.d_coef.ptr(), b.d_flags.ptr(), b.flat.ptr())
         xa, xb = a.snapshot(), b.snapshot()
+        # the stage-2 run against the oracle's own step: state, and the
+        # replica against the oracle's gather of its updated shards
+        prev = H.oracle_state(b.ost)
+        norm, coef, skip, flat = ostep.shard_step(b.op, b.ost, b.grad_bufs, HP, t, 1.0, osc)
+        assert int(b.d_flags.np()[0]) == int(skip)
+        assert np.array_equal(xb["grad_shards"], b.ost.grad_shards)
+        exact = skip or H.same_bits(b.d_coef.np()[0], coef)
+        H.assert_state(xb, b.ost, prev, f"{case} {dtype} stage 2 step {t}", exact)
+        H.assert_16bit(b.flat.u16(), flat, "stage-2 replica", dtype, exact)
+        H.assert_16bit(xb["persist_params"], b.ost.persist_params, "persist_params", dtype, exact)
+        # and against the ZeRO-3 run, bit for bit
         for k in ("master", "exp_avg", "exp_avg_sq", "p_master", "persist_params", "grad_shards"):
             assert np.array_equal(xa[k].view(np.uint8), xb[k].view(np.uint8)), k
         assert np.array_equal(a.flat.u16(), b.flat.u16())
@@ -82,8 +96,6 @@ def test_zero1_gradient_allreduce(case):
     torch.cuda.synchronize()
     got = out.u16()
     N = d.N
-    for b_, ents in enumerate(d.op.reduce_buckets):
-        pass
     # oracle: all-reduce mean of each rank's full gradient, parameter by parameter
     full = {}
     for b_, ents in enumerate(d.op.reduce_buckets):

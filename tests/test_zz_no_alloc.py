@@ -17,6 +17,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import zero_sharded_optimizer_bucket_gb300 as zs  # noqa: E402
+from oracle import step as ostep  # noqa: E402
 from synth import workloads  # noqa: E402
 from tests import gpu_harness as H  # noqa: E402
 
@@ -54,10 +55,24 @@ def test_noalloc_norm_matches_scratch_version_two_calls(case):
         d.set_grads(seed, use_gpu_generator=True)
         d.reduce_scatter_all_buckets(with_scratch=False)
         ref, got = _run_both(d, max_norm)
+        # the same kernels on the same reduced gradients: the same bits
         assert ref[2] == got[2] == 0, f"call {call}"
-        assert abs(got[0] - ref[0]) <= 1e-5 * ref[0], f"call {call}: norm {got[0]} vs {ref[0]}"
-        assert abs(got[1] - ref[1]) <= 1e-5 * ref[1], f"call {call}: coef {got[1]} vs {ref[1]}"
+        assert _bits(got[0]) == _bits(ref[0]), f"call {call}: norm {got[0]!r} vs {ref[0]!r}"
+        assert _bits(got[1]) == _bits(ref[1]), f"call {call}: coef {got[1]!r} vs {ref[1]!r}"
+        # and the oracle's norm of its own reduce-scatter of the same rank
+        # gradients, within the norm tolerance
+        for b in range(len(d.op.reduce_buckets)):
+            ostep.reduce_scatter(d.op, b, d.grad_bufs[b], d.ost)
+        onorm, ocoef, oskip = ostep.grad_norm(d.op, d.ost, max_norm)
+        assert not oskip
+        assert abs(got[0] - float(onorm)) <= 1e-5 * float(onorm), f"call {call}: vs oracle"
+        assert abs(got[1] - float(ocoef)) <= 1e-5 * float(ocoef), f"call {call}: coef vs oracle"
+        assert float(ocoef) < 1.0              # clipping is active
     d.check_canaries()
+
+
+def _bits(x):
+    return int(np.float32(x).view(np.uint32))
 
 
 def test_noalloc_rejects_plans_beyond_the_array():
