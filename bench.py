@@ -333,71 +333,308 @@ def barrier(world: int):
 
 
 # ------------------------------------------------------ CPU baseline ------
-def _sample_params(w, target=4_200_000):
-    """A bounded sample of the workload: the smallest run of parameters in
-    ds_id order, each at most 8M elements, reaching `target` elements."""
+# The oracle (oracle/, plain numpy, one process = one core) timed on the
+# host.  One step of the path over a sample of the workload: the parameters
+# of its first decoder layer (else its first parameters up to a bound).  On
+# several cores the sample is cut into one element range per process; each
+# process holds the oracle's plan and state of its ranges, so that a step is
+#   phase 1: every process reduce-scatters its buckets (oracle.step
+#            reduce_scatter) and returns the counts of its reduced values;
+#   the parent adds the counts and forms the global norm and clip
+#            coefficient (oracle.step sumsq_from_counts, clip_from_sumsq);
+#   phase 2: every process runs Adam (oracle.step adam_step) and its gathers
+#            (oracle.step gather_model).
+# The same oracle functions in the same order as oracle.step.shard_step; the
+# norm is global, as the pages require.  Gradients of a process come from a
+# Philox pool of its own (synth.philox) that its rank buffers index with
+# wrap-around, as the device workload's pool does.
+ORACLE_POOL_ELEMS = 1 << 22
+_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def oracle_sample(w, target=218_112_000):
+    """Indices of the sampled parameters: the parameters of decoder layer 0
+    (all parameters when the list has no layers), in order, leaving out any
+    larger than `target` elements, until `target` elements are reached.
+    The default takes a whole Llama-3-8B layer."""
+    cand = [i for i, n in enumerate(w.names) if n.startswith("layers.0.")]
+    if not cand:
+        cand = list(range(len(w.numel)))
     idx, tot = [], 0
-    for i, n in enumerate(w.numel):
-        if n <= 8_000_000:
+    for i in cand:
+        if w.numel[i] <= target:
             idx.append(i)
-            tot += n
+            tot += w.numel[i]
             if tot >= target:
                 break
     return idx
 
 
-def oracle_step_timer(w, sample_idx, bufs_fn, budget_s, min_steps=1):
-    """Time the oracle's whole step on the sampled parameters."""
+def split_elements(numels, parts):
+    """Cut a list of parameter sizes into `parts` consecutive element ranges
+    of near-equal size; returns, per part, the sizes of its pieces (a
+    parameter cut between two parts becomes one piece in each)."""
+    total = sum(numels)
+    bounds = [total * (k + 1) // parts for k in range(parts)]
+    out, cur, pos, k = [[] for _ in range(parts)], 0, 0, 0
+    for n in numels:
+        left = n
+        while left > 0:
+            take = min(left, bounds[k] - pos)
+            if take > 0:
+                out[k].append(take)
+                pos += take
+                left -= take
+            if pos >= bounds[k] and k < parts - 1:
+                k += 1
+        if n == 0:
+            out[k].append(0)
+    return out
+
+
+def cpu_info():
+    """Host CPU: logical cores, the cores this process may run on, model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    try:
+        allowed = sorted(os.sched_getaffinity(0))
+    except AttributeError:
+        allowed = list(range(os.cpu_count() or 1))
+    return {"nproc": os.cpu_count(), "allowed": allowed, "cpu_model": model}
+
+
+def _oracle_part(spec):
+    """Plan, state and rank gradient buffers of one process's ranges.
+    Weights and gradients are drawn from Philox pools of ORACLE_POOL_ELEMS
+    values (the process's own counters) repeated to the length needed: the
+    distributions of the workload at a bounded generation cost."""
     import numpy as np
 
     from oracle import plan as oplan
     from oracle import step as ostep
     from synth import philox
-    numel = [w.numel[i] for i in sample_idx]
-    plan = oplan.build_partition(numel, w.n_ranks, threshold=w.persistence_threshold,
-                                 reduce_bucket_size=w.reduce_bucket_size,
-                                 prefetch_bucket_size=w.prefetch_bucket_size,
-                                 sub_group_size=w.sub_group_size)
-    W = philox.weight_f32(w.seed, np.arange(plan.input_elems, dtype=np.uint64), w.weight_sigma)
-    st = ostep.partition(plan, W)
-    bufs = bufs_fn(plan)
-    times, t = [], 0
-    t_start = time.perf_counter()
-    while len(times) < min_steps or time.perf_counter() - t_start < budget_s:
-        t += 1
-        t0 = time.perf_counter()
-        ostep.shard_step(plan, st, bufs, w.hparams(), t, w.max_norm)
-        times.append(time.perf_counter() - t0)
-    return plan, times
+    from synth import workloads as wl
+    plan = oplan.build_partition(spec["pieces"], spec["n_ranks"], threshold=spec["threshold"],
+                                 reduce_bucket_size=spec["reduce_bucket_size"],
+                                 prefetch_bucket_size=spec["prefetch_bucket_size"],
+                                 sub_group_size=spec["sub_group_size"], dtype=spec["dtype"],
+                                 shard_group_size=spec["group"] or None)
+    P = spec["pool_elems"]
+    n_w = max(1, min(plan.input_elems, P))
+    W = philox.weight_f32(spec["seed"], spec["w_off"] + np.arange(n_w, dtype=np.uint64),
+                          spec["weight_sigma"])
+    st = ostep.partition(plan, np.resize(W, plan.input_elems))
+    need = sum(plan.n_ranks * ((L + 7) // 8 * 8) for L in plan.bucket_buf_elems)
+    largest = (max(plan.bucket_buf_elems, default=8) + 7) // 8 * 8
+    M = max(8, min(need, max(P, (plan.n_ranks + 1) * largest)))
+    idx = spec["g_off"] + np.arange(min(M, P), dtype=np.uint64)
+    if spec["dtype"] == "fp16":
+        base = philox.grad_fp16(spec["seed"], 0, idx, spec["fp16_log2_scale"])
+    else:
+        base = philox.grad_bf16(spec["seed"], 0, idx, spec["grad_sigma"], spec["outlier_frac"],
+                                spec["outlier_scale"])
+    pool = np.resize(base, M)
+    offs = wl.pool_offsets(plan.bucket_buf_elems, plan.n_ranks, M) if plan.bucket_buf_elems else []
+    bufs = [[pool[o:o + L] for o in offs[b]] for b, L in enumerate(plan.bucket_buf_elems)]
+    return plan, st, bufs
 
 
-def cpu_baseline(w, dw=None, budget_s=12.0):
+def _part_counts(plan, st):
+    """Counts of the |x| bit patterns of a process's reduced gradients
+    (shard and persistent space; padding is zero and adds nothing)."""
     import numpy as np
-    idx = _sample_params(w)
-    N = w.n_ranks
+    c = np.bincount(st.grad_shards.ravel() & np.uint16(0x7FFF), minlength=1 << 15)
+    c += np.bincount(st.persist_grads.ravel() & np.uint16(0x7FFF), minlength=1 << 15)
+    return c.astype(np.int64)
 
-    def bufs_from_device(plan):
-        # inputs for a timing run: gradient buffers copied from the device pool
-        out, off = [], 0
-        pool = dw.pool
-        for L in plan.bucket_buf_elems:
-            row = []
-            for _ in range(N):
-                L8 = _align8(L)
-                if off + L8 > pool.numel():
-                    off = 0
-                row.append(pool[off:off + L].cpu().numpy().view(np.uint16).copy())
-                off += L8
-            out.append(row)
-        return out
 
-    plan, times = oracle_step_timer(w, idx, bufs_from_device, budget_s)
-    sample_psi = plan.psi
-    per = statistics.median(times)
-    return {"value": sample_psi / per, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(idx)} parameters of {w.name} ({sample_psi} elements, N={N}, "
-                      f"{len(plan.reduce_buckets)} reduce buckets): whole oracle step, "
-                      f"{len(times)} steps, median {per:.3f} s, numpy float32 on one core"}
+def _oracle_worker(conn, spec):
+    """One host process of the oracle's parallel step (see above)."""
+    if spec.get("cpu") is not None:
+        try:
+            os.sched_setaffinity(0, {spec["cpu"]})
+        except (AttributeError, OSError):
+            pass
+    from oracle import step as ostep
+    plan, st, bufs = _oracle_part(spec)
+    conn.send(("ready", plan.psi))
+    while True:
+        msg = conn.recv()
+        if msg[0] == "rs":
+            for b in range(len(plan.reduce_buckets)):
+                ostep.reduce_scatter(plan, b, bufs[b], st)
+            conn.send(("counts", _part_counts(plan, st)))
+        elif msg[0] == "adam":
+            _, coef, skip, t = msg
+            ostep.adam_step(plan, -1, spec["hp"], t, coef, skip, st)
+            ostep.gather_model(plan, st.param_shards)
+            conn.send(("done", None))
+        else:
+            conn.send(("bye", None))
+            return
+
+
+def part_specs(w, sample_idx, parts):
+    """What each of `parts` processes holds: its element ranges of the
+    sampled parameters, the workload's settings, and the counter offsets of
+    its weights and gradients."""
+    numels = [w.numel[i] for i in sample_idx]
+    specs, w_off, g_off = [], 0, 0
+    for pieces in split_elements(numels, parts):
+        specs.append(dict(pieces=pieces, n_ranks=w.n_ranks, threshold=w.persistence_threshold,
+                          reduce_bucket_size=w.reduce_bucket_size,
+                          prefetch_bucket_size=w.prefetch_bucket_size,
+                          sub_group_size=w.sub_group_size, dtype=w.dtype,
+                          group=w.shard_group_size, seed=w.seed, weight_sigma=w.weight_sigma,
+                          grad_sigma=w.grad_sigma, outlier_frac=w.outlier_frac,
+                          outlier_scale=w.outlier_scale, fp16_log2_scale=w.fp16_log2_scale,
+                          hp=w.hparams(), w_off=w_off, g_off=g_off,
+                          pool_elems=ORACLE_POOL_ELEMS, cpu=None))
+        w_off += sum(pieces)
+        g_off += ORACLE_POOL_ELEMS
+    return specs
+
+
+class OracleCluster:
+    """The oracle's step on `cpus` host processes (spawned, one pinned to
+    each listed core), each over one element range of the sampled
+    parameters."""
+
+    def __init__(self, w, sample_idx, cpus):
+        import multiprocessing as mp
+
+        self.cpus = list(cpus)
+        self.w = w
+        specs = part_specs(w, sample_idx, len(self.cpus))
+        self.psi = sum(sum(sp["pieces"]) for sp in specs)
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        # one thread per process (the children inherit the environment)
+        saved = {v: os.environ.get(v) for v in _THREAD_VARS}
+        os.environ.update({v: "1" for v in _THREAD_VARS})
+        try:
+            for spec, cpu in zip(specs, self.cpus):
+                a, b = ctx.Pipe()
+                proc = ctx.Process(target=_oracle_worker, args=(b, dict(spec, cpu=cpu)),
+                                   daemon=True)
+                proc.start()
+                self.conns.append(a)
+                self.procs.append(proc)
+        finally:
+            for v, x in saved.items():
+                if x is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = x
+        for c in self.conns:
+            tag, _ = c.recv()
+            assert tag == "ready"
+        self.t = 0
+        self.scale = float(w.loss_scale) if w.dtype == "fp16" else 1.0
+
+    def step(self):
+        """One parallel oracle step; returns (norm, coef, skip)."""
+        import numpy as np
+
+        from oracle import step as ostep
+        self.t += 1
+        for c in self.conns:
+            c.send(("rs",))
+        counts = np.zeros(1 << 15, dtype=np.int64)
+        for c in self.conns:
+            counts += c.recv()[1]
+        norm, coef, skip = ostep.clip_from_sumsq(ostep.sumsq_from_counts(counts, self.w.dtype),
+                                                 self.w.max_norm, self.scale)
+        for c in self.conns:
+            c.send(("adam", coef, skip, self.t))
+        for c in self.conns:
+            c.recv()
+        return norm, coef, skip
+
+    def close(self):
+        for c, p in zip(self.conns, self.procs):
+            try:
+                c.send(("stop",))
+                c.recv()
+            except (OSError, EOFError):
+                pass
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+
+
+def time_oracle(w, sample_idx, cpus, budget_s, min_steps=2, warmup=1):
+    """Median seconds per parallel oracle step over at least min_steps
+    steps and about budget_s seconds, after `warmup` untimed steps."""
+    cl = OracleCluster(w, sample_idx, cpus)
+    try:
+        for _ in range(warmup):
+            cl.step()
+        times = []
+        t_start = time.perf_counter()
+        while len(times) < min_steps or time.perf_counter() - t_start < budget_s:
+            t0 = time.perf_counter()
+            cl.step()
+            times.append(time.perf_counter() - t0)
+        return cl.psi, times
+    finally:
+        cl.close()
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The oracle on the host: one core on a 1/16 slice of the sample, and
+    every core this process may use on the whole sample."""
+    info = cpu_info()
+    idx = oracle_sample(w)
+    cpus = info["allowed"]
+    one_idx = idx
+    psi_all, t_all = time_oracle(w, idx, cpus, budget_s)
+    # one core: the same per-process share of the sample as one of the
+    # all-core processes (a process holds psi / len(cpus) elements)
+    sub = split_elements([w.numel[i] for i in one_idx], max(len(cpus), 1))[0]
+    from synth import workloads as wl
+    w1 = wl.Workload(w.name, w.n_ranks, [f"piece{i}" for i in range(len(sub))],
+                     [(n,) for n in sub], **{k: getattr(w, k) for k in _WL_FIELDS})
+    psi_1, t_1 = time_oracle(w1, list(range(len(sub))), cpus[:1], budget_s)
+    per_all, per_1 = statistics.median(t_all), statistics.median(t_1)
+    names = [w.names[i] for i in idx]
+    what = ("decoder layer 0 (" + ", ".join(n.split(".")[-1] for n in names) + ")"
+            if names and names[0].startswith("layers.0.") else f"{len(idx)} parameters")
+    return {"value": psi_all / per_all, "unit": UNIT, "cores": len(cpus), "kind": "oracle",
+            "sample": f"{what} of {w.name}: {psi_all} elements, N={w.n_ranks}; the whole oracle "
+                      f"step (reduce-scatter, global norm, Adam, gathers) on {len(cpus)} "
+                      f"processes, one element range each, median of {len(t_all)} steps "
+                      f"({per_all:.3f} s)",
+            "nproc": info["nproc"], "cpu_model": info["cpu_model"],
+            "cores_all": {"value": psi_all / per_all, "cores": len(cpus), "psi": psi_all,
+                          "s_per_step": per_all, "steps": len(t_all)},
+            "cores_1": {"value": psi_1 / per_1, "cores": 1, "psi": psi_1, "s_per_step": per_1,
+                        "steps": len(t_1),
+                        "sample": f"the first of the {len(cpus)} element ranges ({psi_1} "
+                                  f"elements) on one core"},
+            "parallel_efficiency": (psi_all / per_all) / (len(cpus) * psi_1 / per_1)}
+
+
+_WL_FIELDS = ("persistence_threshold", "reduce_bucket_size", "prefetch_bucket_size",
+              "sub_group_size", "grad_sigma", "outlier_frac", "outlier_scale", "weight_sigma",
+              "steps", "lr", "beta1", "beta2", "eps", "weight_decay", "adamw", "max_norm", "seed",
+              "dtype", "fp16_log2_scale", "loss_scale", "scale_window", "shard_group_size")
 
 
 # ------------------------------------------------------------- e2e --------
@@ -609,7 +846,7 @@ def run_gpu(args):
     if not args.no_e2e:
         res["e2e"] = run_e2e(dw, steps=args.e2e_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, dw, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -619,59 +856,38 @@ def run_gpu(args):
 
 def run_reference(args):
     """The oracle as it stands, on the host cores, same metric and workload:
-    each step is the oracle's whole step on a bounded sample of the
-    workload's parameters (inputs drawn on the CPU by synth.philox)."""
+    each step is the oracle's whole step (oracle.step functions, parallel
+    over the host's cores as in cpu_baseline) on a bounded sample of the
+    workload (its first decoder layer, else its first parameters)."""
     rank, world, _ = dist_setup()
     if rank != 0:
         return
-    import numpy as np
-
-    from synth import philox
     w = load_workload(args.workload)
-    idx = _sample_params(w, target=2_000_000)
-    N = w.n_ranks
-
-    def bufs_cpu(plan):
-        out, run = [], 0
-        for L in plan.bucket_buf_elems:
-            row = []
-            for _ in range(N):
-                row.append(philox.grad_bf16(w.seed, 0, np.arange(run, run + L, dtype=np.uint64),
-                                            w.grad_sigma, w.outlier_frac, w.outlier_scale))
-                run += _align8(L)
-            out.append(row)
-        return out
-
-    from oracle import plan as oplan
-    from oracle import step as ostep
-    numel = [w.numel[i] for i in idx]
-    plan = oplan.build_partition(numel, N, threshold=w.persistence_threshold,
-                                 reduce_bucket_size=w.reduce_bucket_size,
-                                 prefetch_bucket_size=w.prefetch_bucket_size,
-                                 sub_group_size=w.sub_group_size)
-    Wt = philox.weight_f32(w.seed, np.arange(plan.input_elems, dtype=np.uint64), w.weight_sigma)
-    st = ostep.partition(plan, Wt)
-    bufs = bufs_cpu(plan)
-    t = 0
-    for _ in range(args.warmup):
-        t += 1
-        ostep.shard_step(plan, st, bufs, w.hparams(), t, w.max_norm)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        t += 1
-        ostep.shard_step(plan, st, bufs, w.hparams(), t, w.max_norm)
-    dt = (time.perf_counter() - t0) / args.steps
-    value = plan.psi / dt
-    sample = (f"{len(idx)} parameters of {w.name} ({plan.psi} elements, N={N}): whole oracle "
-              f"step per timed step, numpy float32, one core")
+    info = cpu_info()
+    cpus = info["allowed"]
+    idx = oracle_sample(w, target=args.reference_sample)
+    cl = OracleCluster(w, idx, cpus)
+    try:
+        for _ in range(args.warmup):
+            cl.step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            cl.step()
+        dt = (time.perf_counter() - t0) / args.steps
+    finally:
+        cl.close()
+    value = cl.psi / dt
+    sample = (f"{len(idx)} parameters of {w.name} ({cl.psi} elements, N={w.n_ranks}): whole "
+              f"oracle step per timed step on {len(cpus)} host processes, one element range "
+              f"each (numpy float32)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": {"workload": w.name, "n_ranks": N, "psi": w.psi,
-                                        "sample_psi": plan.psi},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "data": "synthetic", "config": {"workload": w.name, "n_ranks": w.n_ranks, "psi": w.psi,
+                                        "sample_psi": cl.psi},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(cpus), "kind": "oracle",
+                         "sample": sample, "nproc": info["nproc"], "cpu_model": info["cpu_model"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -863,7 +1079,11 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of timed oracle steps per CPU-baseline leg")
+    ap.add_argument("--reference-sample", type=int, default=50_000_000,
+                    help="--impl reference: elements of the sampled parameters (bounded so "
+                         "that a warm-up + timed run ends within minutes)")
     ap.add_argument("--gather-schedule", action="store_true",
                     help="measure the forward/backward gather scheduler instead of the step")
     ap.add_argument("--gather-compute", default="busy", choices=["busy", "gemm"],

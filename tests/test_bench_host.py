@@ -8,6 +8,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -59,9 +60,65 @@ def test_sample_is_bounded():
     import bench
     from synth import workloads
     w = workloads.llama3_8b()
-    idx = bench._sample_params(w)
-    tot = sum(w.numel[i] for i in idx)
-    assert 4_000_000 <= tot <= 16_000_000 and all(w.numel[i] <= 8_000_000 for i in idx)
+    idx = bench.oracle_sample(w)
+    assert [w.names[i] for i in idx][0] == "layers.0.q_proj"
+    assert sum(w.numel[i] for i in idx) == 218_112_000         # one whole decoder layer
+    idx = bench.oracle_sample(w, target=50_000_000)
+    assert all(w.numel[i] <= 50_000_000 for i in idx) and sum(w.numel[i] for i in idx) < 5e7
+    w = workloads.many_small()
+    assert 218_112_000 <= sum(w.numel[i] for i in bench.oracle_sample(w)) < 220_000_000
+
+
+def test_split_elements_covers_every_element_once():
+    sys.path.insert(0, ROOT)
+    import bench
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        numels = [int(x) for x in rng.integers(0, 1000, size=int(rng.integers(0, 12)))]
+        P = int(rng.integers(1, 9))
+        parts = bench.split_elements(numels, P)
+        assert len(parts) == P
+        flat = [n for part in parts for n in part]
+        assert sum(flat) == sum(numels) and all(n >= 0 for n in flat)
+        sizes = [sum(part) for part in parts]
+        assert max(sizes, default=0) - min(sizes, default=0) <= 1
+        # the pieces are the parameters cut at the part boundaries, in order
+        cuts = np.cumsum([0] + [n for n in numels if n])
+        edges = np.cumsum([0] + [n for n in flat if n])
+        assert set(cuts.tolist()) <= set(edges.tolist())
+
+
+def test_parallel_oracle_step_uses_the_global_norm():
+    """The oracle's step on 2 host processes: the norm the parent forms from
+    the processes' counts is the norm of both processes' reduced gradients
+    together, computed here in one process from the same inputs."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import step as ostep
+    from synth import workloads
+    w = workloads.tiny(threshold=100)
+    w.max_norm = 0.05
+    idx = bench.oracle_sample(w)
+    cl = bench.OracleCluster(w, idx, [None, None])
+    try:
+        got = cl.step()
+    finally:
+        cl.close()
+    sq = 0.0
+    counts = np.zeros(1 << 15, dtype=np.int64)
+    for spec in bench.part_specs(w, idx, 2):
+        plan, st, bufs = bench._oracle_part(spec)
+        for b in range(len(plan.reduce_buckets)):
+            ostep.reduce_scatter(plan, b, bufs[b], st)
+        x = np.concatenate([ostep.to_f32(st.grad_shards).ravel(),
+                            ostep.to_f32(st.persist_grads).ravel()]).astype(np.float64)
+        sq += float(np.sum(x * x))
+        counts += bench._part_counts(plan, st)
+    ref = ostep.clip_from_sumsq(ostep.sumsq_from_counts(counts), w.max_norm)
+    assert got[2] is False and got[1] < 1.0
+    assert np.float32(got[0]).tobytes() == np.float32(ref[0]).tobytes()
+    assert np.float32(got[1]).tobytes() == np.float32(ref[1]).tobytes()
+    assert abs(float(got[0]) - np.sqrt(sq)) <= 1e-6 * np.sqrt(sq)
 
 
 @pytest.mark.slow
