@@ -197,6 +197,48 @@ class DeviceWorkload:
             launches += (len(ps) + 127) // 128
         return launches
 
+    def layer_ranges(self):
+        """Runs of consecutive reduce buckets whose gradients one backward
+        block produces together: the buckets whose first parameter lies in
+        the same decoder layer (the embedding and the output head apart);
+        lists without layers take runs of 32 buckets."""
+        zs, w = self.zs, self.w
+        nb = len(self.buf_elems)
+        keys = []
+        for b in range(nb):
+            first = zs.zs_bucket_entry(self.plan, b, 0)[0]
+            name = w.names[first]
+            keys.append(name.split(".")[1] if name.startswith("layers.") else
+                        name if any(n.startswith("layers.") for n in w.names) else b // 32)
+        runs, a = [], 0
+        for b in range(1, nb + 1):
+            if b == nb or keys[b] != keys[a]:
+                runs.append((a, b - a))
+                a = b
+        return runs
+
+    def unfused_ranges_step(self):
+        """unfused_step with the reduce-scatter issued as one
+        zs_reduce_scatter_range per run of layer_ranges()."""
+        zs = self.zs
+        if not hasattr(self, "_runs"):
+            self._runs = self.layer_ranges()
+            self.unfused_step()          # sets up the gather lists
+            self.t -= 1
+        self.t += 1
+        N = self.N
+        for a, n in self._runs:
+            zs.zs_reduce_scatter_range(self.plan, a, n, self.ptr_table[a * N:], self.gs, self.gP,
+                                       self.scratch)
+        self.norm()
+        for sg in range(self.info["n_sub_groups"]):
+            zs.zs_adam_step(self.plan, sg, self.hp, self.t, self.d_coef, self.d_flags, self.state)
+        launches = len(self._runs) + 2 + self.info["n_sub_groups"]
+        for ps, base, n in self._gathers:
+            zs.zs_all_gather_coalesced(self.plan, ps, self.ps, base, n)
+            launches += (len(ps) + 127) // 128
+        return launches
+
     def algorithmic_bytes(self):
         """Bytes the method must move per step (padding excluded):
         reduce-scatter 2N + 2 per element; Adam + cast 28 per element plus
@@ -826,6 +868,18 @@ def run_gpu(args):
                       "launches_per_step": n_unfused,
                       "calls": "zs_reduce_scatter per bucket, zs_grad_norm, zs_adam_step per "
                                "sub-group, zs_all_gather_coalesced per gather bucket"}
+    dw.unfused_ranges_step()
+    torch.cuda.synchronize(dev)
+    u0.record()
+    for _ in range(KU):
+        n_ranged = dw.unfused_ranges_step()
+    u1.record()
+    torch.cuda.synchronize(dev)
+    res["unfused_ranges"] = {"ms_per_step": u0.elapsed_time(u1) / KU, "steps": KU,
+                             "launches_per_step": n_ranged, "ranges": len(dw._runs),
+                             "calls": "zs_reduce_scatter_range per decoder layer's buckets, "
+                                      "then as unfused"}
+    res["unfused_bytes_per_elem"] = 2 * dw.N + 36
     # ZeRO-2 residency: no shard buffer, the parameters live in the replica
     st2 = dw.zs.make_state(grad_shards=dw.gs, param_shards=None, master=dw.master, exp_avg=dw.m,
                            exp_avg_sq=dw.v, persist_grads=dw.gP, persist_params=dw.pP,

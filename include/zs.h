@@ -430,6 +430,24 @@ zs_status zs_device_wait_timeouts(int32_t *count, int32_t reset);
  * no counterpart in the pages.  Errors: ZS_EINVAL (limit), ZS_ECUDA. */
 zs_status zs_test_wait_timeout(int64_t limit_ns, void *stream);
 
+/* A2 over the consecutive buckets [first_bucket, first_bucket + n_buckets)
+ * in one launch, for buckets that become ready back to back ([ZeRO-3
+ * chapter] §6.2: a full IPG bucket is reduced and scattered; when several
+ * fill at once, as at the end of the backward pass, one launch takes them
+ * all).  Same result as zs_reduce_scatter on each of those buckets in turn.
+ * Separate zs_reduce_scatter calls keep stream order: each waits for the
+ * kernel before it to finish, which leaves the GPU partly idle while the
+ * previous bucket's last tiles drain; a range has no such gap inside it.
+ * d_rank_grads: DEVICE array [n_buckets][N] of device pointers (rank k's
+ * buffer of bucket first_bucket + i at [i*N + k]; 16-byte aligned; a NULL
+ * or misaligned entry is not read and makes that tile's norm partial NaN).
+ * norm_scratch (NULL, or >= norm_scratch_elems doubles) receives the
+ * tiles' partial sums.  n_buckets = 0 enqueues nothing.  Errors: ZS_EINVAL
+ * (range outside the plan, pointers), ZS_ESTATE, ZS_ECUDA. */
+zs_status zs_reduce_scatter_range(const zs_plan *plan, int32_t first_bucket, int32_t n_buckets,
+                                  const void *const *d_rank_grads, void *grad_shards,
+                                  void *persist_grads, double *norm_scratch, void *stream);
+
 /* A2 over every bucket in one launch — the first pass of zs_shard_step.
  * Same result as zs_reduce_scatter on each bucket in turn.  d_rank_grads
  * as in zs_shard_step; norm_scratch (>= norm_scratch_elems doubles) receives

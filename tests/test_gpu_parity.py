@@ -124,6 +124,86 @@ def test_grad_norm(case):
     d.check_canaries()
 
 
+def test_reduce_scatter_ranges(case):
+    """zs_reduce_scatter_range over random runs of consecutive buckets: the
+    reduced gradients bit for bit as the oracle's, the partial sums the
+    same bits as the recomputed ones; ranges outside the plan are argument
+    errors."""
+    d = make(case)
+    d.init_weights()
+    d.set_grads(123, use_gpu_generator=(case == "many_small_64"))
+    nb = len(d.op.reduce_buckets)
+    rng = np.random.default_rng(nb)
+    cuts = sorted({0, nb, *[int(x) for x in rng.integers(0, nb + 1, size=min(nb, 5))]})
+    N = d.N
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        zs.zs_reduce_scatter_range(d.plan, a, b - a, d.ptr_table[a * N:],
+                                   d.bufs["grad_shards"].ptr(), d.bufs["persist_grads"].ptr(),
+                                   d.scratch.ptr())
+    zs.zs_reduce_scatter_range(d.plan, nb, 0, None, d.bufs["grad_shards"].ptr(),
+                               d.bufs["persist_grads"].ptr(), None)          # empty: nothing
+    for b in range(nb):
+        ostep.reduce_scatter(d.op, b, d.grad_bufs[b], d.ost)
+    s = d.snapshot()
+    assert np.array_equal(s["grad_shards"], d.ost.grad_shards)
+    assert np.array_equal(s["persist_grads"], d.ost.persist_grads)
+    d.grad_norm(1.0, recompute=False)
+    n1 = float(d.d_norm.np()[0])
+    d.grad_norm(1.0, recompute=True)
+    assert H.same_bits(n1, d.d_norm.np()[0])
+    for first, n in [(-1, 1), (0, nb + 1), (nb, 1)]:
+        with pytest.raises(zs.ZsError):
+            zs.zs_reduce_scatter_range(d.plan, first, n, d.ptr_table,
+                                       d.bufs["grad_shards"].ptr(),
+                                       d.bufs["persist_grads"].ptr(), None)
+    d.check_canaries()
+
+
+@pytest.mark.parametrize("kind", ["huge", "tiny_tensor", "all_tiny"])
+def test_grad_norm_out_of_range_values(kind):
+    """Values whose squares leave float32's exact range send their tiles to
+    the float64 sum: a few gradients of 2^70 (squares overflow float32), one
+    whole tensor of 2^-100 (squares underflow), every gradient 2^-100.  The
+    norm from the reduce-scatter's partials and the recomputed one keep the
+    same bits, and both match the oracle's exactly rounded norm."""
+    d = make("ragged_n16_chunks")
+    d.init_weights()
+    d.set_grads(55)
+    big, tiny = 0x6280, 0x0D80              # bf16 bits of 2^70 and 2^-100
+    host = d.pool.cpu().numpy().view(np.uint16)
+    if kind == "huge":
+        for b, k, i in [(0, 0, 3), (1, 5, 0), (len(d.grad_bufs) - 1, 15, 7)]:
+            host[d.ptrs[b][k] // 2 - d.pool.data_ptr() // 2 + i] = big
+    elif kind == "tiny_tensor":
+        ent = d.op.reduce_buckets[2][0]
+        for k in range(d.N):
+            o = d.ptrs[2][k] // 2 - d.pool.data_ptr() // 2 + ent.buf_off
+            host[o:o + ent.e_hi - ent.e_lo] = tiny
+    else:
+        host[:] = tiny
+    d.pool.copy_(torch.from_numpy(host.view(np.int16).copy()))
+    for b in range(len(d.grad_bufs)):
+        for k in range(d.N):
+            o = d.ptrs[b][k] // 2 - d.pool.data_ptr() // 2
+            d.grad_bufs[b][k] = host[o:o + len(d.grad_bufs[b][k])].copy()
+    d.reduce_scatter_all_buckets(with_scratch=True)
+    for b in range(len(d.op.reduce_buckets)):
+        ostep.reduce_scatter(d.op, b, d.grad_bufs[b], d.ost)
+    assert np.array_equal(d.snapshot()["grad_shards"], d.ost.grad_shards)
+    d.grad_norm(1.0, recompute=False)
+    n1, c1 = float(d.d_norm.np()[0]), float(d.d_coef.np()[0])
+    d.grad_norm(1.0, recompute=True)
+    n2, c2 = float(d.d_norm.np()[0]), float(d.d_coef.np()[0])
+    assert H.same_bits(n1, n2) and H.same_bits(c1, c2)
+    norm, coef, skip = ostep.grad_norm(d.op, d.ost, 1.0)
+    assert not skip and int(d.d_flags.np()[0]) == 0
+    print(f"{kind}: norm {n1!r} (oracle {float(norm)!r})")
+    assert abs(n1 - float(norm)) <= 1e-5 * float(norm)
+    assert abs(c1 - float(coef)) <= 1e-5 * float(coef)
+    assert zs.zs_device_wait_timeouts() == 0
+    d.check_canaries()
+
+
 def test_adam_isolated_bit_exact(case):
     """Adam on the device with the oracle's clip coefficient: the same fp32
     operations in the same order, so the same bits."""

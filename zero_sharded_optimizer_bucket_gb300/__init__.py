@@ -151,6 +151,7 @@ _sig("zs_all_gather_coalesced", _i32, [_P, _i32, C.POINTER(_i32), _P, _P, _i64, 
 _sig("zs_device_wait_timeouts", _i32, [C.POINTER(_i32), _i32])
 _sig("zs_test_wait_timeout", _i32, [_i64, _P])
 _sig("zs_reduce_scatter_all", _i32, [_P, _P, _P, _P, _P, _P])
+_sig("zs_reduce_scatter_range", _i32, [_P, _i32, _i32, _P, _P, _P, _P, _P])
 _sig("zs_adam_gather", _i32, [_P, C.POINTER(zs_adam_hparams), _i64, _P, _P,
                               C.POINTER(zs_shard_state), _P, _P])
 _sig("zs_grad_norm_noalloc", _i32, [_P, _P, _P, _f32, _P, _P, _P, _P])
@@ -415,6 +416,14 @@ def zs_reduce_scatter_all(plan, d_rank_grads, grad_shards, persist_grads, norm_s
     _check(_lib.zs_reduce_scatter_all(_h(plan), _ptr(d_rank_grads), _ptr(grad_shards),
                                       _ptr(persist_grads), _ptr(norm_scratch), _stream(stream)),
            "zs_reduce_scatter_all")
+
+
+def zs_reduce_scatter_range(plan, first_bucket: int, n_buckets: int, d_rank_grads, grad_shards,
+                            persist_grads, norm_scratch, stream=None) -> None:
+    _check(_lib.zs_reduce_scatter_range(_h(plan), int(first_bucket), int(n_buckets),
+                                        _ptr(d_rank_grads), _ptr(grad_shards), _ptr(persist_grads),
+                                        _ptr(norm_scratch), _stream(stream)),
+           "zs_reduce_scatter_range")
 
 
 def zs_adam_gather(plan, hp, step: int, d_clip_coef, d_flags, state: zs_shard_state, flat_out,

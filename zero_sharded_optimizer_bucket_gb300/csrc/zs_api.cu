@@ -328,26 +328,55 @@ zs_status zs_unscale_and_clip(const zs_plan *P, const void *grad_shards, const v
                                 (cudaStream_t)stream), fn);
 }
 
-zs_status zs_reduce_scatter_all(const zs_plan *P, const void *const *d_rank_grads,
-                                void *grad_shards, void *persist_grads, double *norm_scratch,
-                                void *stream) {
-    const char *fn = "zs_reduce_scatter_all";
+// zs_reduce_scatter_range / zs_reduce_scatter_all; fn names the caller.
+static zs_status rs_range(const zs_plan *P, int32_t first_bucket, int32_t n_buckets,
+                          const void *const *d_rank_grads, void *grad_shards, void *persist_grads,
+                          double *norm_scratch, bool scratch_required, void *stream,
+                          const char *fn) {
     zs_status r = need_table(P, fn);
     if (r) return r;
+    const int64_t nb = (int64_t)P->buckets.size();
+    if (first_bucket < 0 || n_buckets < 0 || (int64_t)first_bucket + n_buckets > nb)
+        return zs_fail(ZS_EINVAL, "%s: buckets [%d, %d + %d) not within the plan's %lld", fn,
+                       first_bucket, first_bucket, n_buckets, (long long)nb);
     if (P->cfg.n_ranks > ZS_MAX_RANKS)
         return zs_fail(ZS_EINVAL, "%s: N = %d > ZS_MAX_RANKS", fn, P->cfg.n_ranks);
-    if (!P->buckets.empty() && !al(d_rank_grads, 8))
+    if (n_buckets > 0 && !al(d_rank_grads, 8))
         return zs_fail(ZS_EINVAL, "%s: d_rank_grads NULL or misaligned", fn);
     if (P->S > 0 && !al(grad_shards, 16))
         return zs_fail(ZS_EINVAL, "%s: grad_shards NULL or not 16-byte aligned", fn);
     if (P->Pn_alloc > 0 && !al(persist_grads, 16))
         return zs_fail(ZS_EINVAL, "%s: persist_grads NULL or not 16-byte aligned", fn);
-    if ((r = check_scratch(P, norm_scratch, fn))) return r;
-    return cuda_status(zsl_reduce_scatter_all(P->d_tiles, (int64_t)P->tiles.size(), d_rank_grads,
-                                              P->cfg.n_ranks, P->G, P->cfg.dtype,
+    if ((scratch_required || norm_scratch) && (r = check_scratch(P, norm_scratch, fn))) return r;
+    if (n_buckets == 0) {
+        zs_clear_error();
+        return ZS_OK;
+    }
+    // the tiles of consecutive buckets are consecutive in the table
+    const ZsBucket &b0 = P->buckets[first_bucket];
+    const ZsBucket &b1 = P->buckets[first_bucket + n_buckets - 1];
+    const int64_t tile0 = b0.first_tile, ntiles = b1.first_tile + b1.n_tiles - b0.first_tile;
+    return cuda_status(zsl_reduce_scatter_all(P->d_tiles, tile0, ntiles, first_bucket,
+                                              d_rank_grads, P->cfg.n_ranks, P->G, P->cfg.dtype,
                                               static_cast<uint16_t *>(grad_shards),
-                                              static_cast<uint16_t *>(persist_grads), norm_scratch,
-                                              (cudaStream_t)stream), fn);
+                                              static_cast<uint16_t *>(persist_grads),
+                                              norm_scratch, (cudaStream_t)stream), fn);
+}
+
+zs_status zs_reduce_scatter_range(const zs_plan *P, int32_t first_bucket, int32_t n_buckets,
+                                  const void *const *d_rank_grads, void *grad_shards,
+                                  void *persist_grads, double *norm_scratch, void *stream) {
+    return rs_range(P, first_bucket, n_buckets, d_rank_grads, grad_shards, persist_grads,
+                    norm_scratch, false, stream, "zs_reduce_scatter_range");
+}
+
+zs_status zs_reduce_scatter_all(const zs_plan *P, const void *const *d_rank_grads,
+                                void *grad_shards, void *persist_grads, double *norm_scratch,
+                                void *stream) {
+    const char *fn = "zs_reduce_scatter_all";
+    if (!P) return zs_fail(ZS_EINVAL, "%s: NULL plan", fn);
+    return rs_range(P, 0, (int32_t)P->buckets.size(), d_rank_grads, grad_shards, persist_grads,
+                    norm_scratch, true, stream, fn);
 }
 
 zs_status zs_adam_gather(const zs_plan *P, const zs_adam_hparams *hp, int64_t step,

@@ -98,36 +98,6 @@ constexpr uint64_t BULK_WAIT_NS = 1000000000ull;       // one wait gives up afte
 
 __device__ int g_bulk_wait_timeouts;                    // waits that gave up
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for the phase of parity `parity` of the mbarrier at shared address
-// bar to complete; false when limit_ns pass first (the clock is read every
-// 64 polls; a poll count far beyond any such time is a second bound).
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = global_ns();
-    for (long long i = 0; i < (1ll << 34); ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 63) == 63 && global_ns() - t0 > limit_ns) return false;
-    }
-    return false;
-}
-
 // Issues the loads of chunk c (output elements [f, f_end)) into stage buffer
 // dst, completing on mbarrier bar; returns the chunk's bytes.
 __device__ uint32_t bulk_load_chunk(const ZsGatherArgs &a, const uint16_t *shards, int64_t c,

@@ -24,9 +24,12 @@ cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t nti
                                const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
                                uint16_t *gP, double *partials, cudaStream_t s);
 
-cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
-                                   const void *const *d_table, int N, int G, int dtype, uint16_t *gs,
-                                   uint16_t *gP, double *partials, cudaStream_t s);
+// Tiles [tile0, tile0 + ntiles) (whole buckets from bucket0 on); rank k's
+// buffer of bucket b at d_table[(b - bucket0) * N + k].
+cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+                                   int32_t bucket0, const void *const *d_table, int N, int G,
+                                   int dtype, uint16_t *gs, uint16_t *gP, double *partials,
+                                   cudaStream_t s);
 
 cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,
                      const uint16_t *gs, const uint16_t *gP, double *scratch, bool recompute,

@@ -10,6 +10,9 @@
 // result is bit-exact against the fixed-order definition.  Five CTAs of 256
 // threads per SM (registers capped by the launch bounds) keep enough loads
 // in flight to stream the N gradient buffers near the HBM read bandwidth.
+#include <algorithm>
+#include <atomic>
+
 #include "zs_device.cuh"
 #include "zs_launch.h"
 
@@ -22,27 +25,42 @@ struct RankPtrs {
 template <bool FROM_TABLE, class T, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 5)
 rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
-          const uint16_t *const *__restrict__ table, int N, int G, float fN,
+          const uint16_t *const *__restrict__ table, int32_t bucket0, int N, int G, float fN,
           uint16_t *__restrict__ gs, uint16_t *__restrict__ gP, double *__restrict__ partials) {
     __shared__ const uint16_t *sp[ZS_MAX_RANKS];
     __shared__ SqRed red;
-    __shared__ int bad;
-    // Launched as a programmatic dependent: wait until the previous kernel
-    // of the stream has finished and its writes are visible (a no-op in an
-    // ordinary launch), then let the next dependent launch start placing
-    // its CTAs, which wait the same way.
+    __shared__ int badw[WARPS];
+    // the tile's results in destination order (the window of the tile norm)
+    __shared__ __align__(16) uint16_t win[NORM_WIN_ELEMS];
+    const int64_t t = tile0 + blockIdx.x;
+    if (!FROM_TABLE && threadIdx.x == 0) {
+        // a per-bucket launch is a programmatic dependent: fetch the tile
+        // descriptor (the plan's table, which no kernel writes) into L1
+        // while the previous kernel finishes
+        const char *d = reinterpret_cast<const char *>(tiles + t);
+        asm volatile("prefetch.global.L1 [%0];" : : "l"(d));
+        asm volatile("prefetch.global.L1 [%0];" : : "l"(d + sizeof(ZsTile) - 1));
+    }
+    // Wait until the previous kernel of the stream has finished and its
+    // writes are visible (a no-op in an ordinary launch), then let the next
+    // dependent launch start placing its CTAs, which wait the same way.
     asm volatile("griddepcontrol.wait;" : : : "memory");
     asm volatile("griddepcontrol.launch_dependents;" : : : "memory");
-    const int64_t t = tile0 + blockIdx.x;
     const ZsTile tile = tiles[t];
-    if (threadIdx.x == 0) bad = 0;
-    __syncthreads();
+    // stage the rank pointers; one barrier, with a per-warp vote on their use
+    int my_bad = 0;
     for (int k = threadIdx.x; k < N; k += THREADS) {
-        const uint16_t *q = FROM_TABLE ? table[(int64_t)tile.bucket * N + k] : ptrs.p[k];
-        if (q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u)) bad = 1;
+        const uint16_t *q =
+            FROM_TABLE ? table[(int64_t)(tile.bucket - bucket0) * N + k] : ptrs.p[k];
+        my_bad |= (q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u)) ? 1 : 0;
         sp[k] = q;
     }
+    my_bad = __any_sync(0xFFFFFFFFu, my_bad);
+    if ((threadIdx.x & 31) == 0) badw[threadIdx.x >> 5] = my_bad;
     __syncthreads();
+    int bad = 0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) bad |= badw[w];
     if (bad) {
         // an unusable rank pointer: read nothing, poison the norm so that
         // the update of this step is skipped
@@ -68,7 +86,9 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     // far cheaper than an IEEE division.  Other N divide.
     const bool pow2 = (N & (N - 1)) == 0;
     const float invN = 1.0f / fN;
-    SqAcc sq;
+    // the norm partial is formed from a shared-memory copy of the results
+    const bool keep = partials != nullptr;
+    const int64_t w0 = D & ~int64_t(7);
     // uniform trip count: every lane takes part in the shuffles
     for (int64_t base = 0; base < nchunks; base += THREADS) {
         const int64_t gi = base + threadIdx.x;
@@ -139,16 +159,19 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             r[i] = act ? T::from_f32(pow2 ? __fmul_rn(acc[i], invN) : __fdiv_rn(acc[i], fN)) : 0u;
-        if (act) group_sq<T>(r, sq);
         const int64_t y0 = 8 * c - delta;  // destination of lane 0 of the chunk
         if (a == 0) {
             if (act) {
                 if (lo <= 0 && hi >= 8) {
                     *reinterpret_cast<uint4 *>(out + y0) = pack8(r);
+                    if (keep) *reinterpret_cast<uint4 *>(win + (y0 - w0)) = pack8(r);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (i >= lo && i < hi) out[y0 + i] = (uint16_t)r[i];
+                        if (i >= lo && i < hi) {
+                            out[y0 + i] = (uint16_t)r[i];
+                            if (keep) win[y0 + i - w0] = (uint16_t)r[i];
+                        }
                 }
             }
         } else {
@@ -161,14 +184,21 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
             const bool next_act = __shfl_down_sync(0xFFFFFFFFu, (int)act, 1) != 0 && lane < 31;
             // my lanes [8-a, 8) and the next chunk's lanes [0, 8-a) all valid
             const bool vec = act && next_act && lo <= 8 - a && hi >= 16 - a;
-            if (vec) *reinterpret_cast<uint4 *>(out + y0 + 8 - a) = shift8(w, wn, 8 - a);
+            if (vec) {
+                const uint4 sv = shift8(w, wn, 8 - a);
+                *reinterpret_cast<uint4 *>(out + y0 + 8 - a) = sv;
+                if (keep) *reinterpret_cast<uint4 *>(win + (y0 + 8 - a - w0)) = sv;
+            }
             const bool prev_vec = __shfl_up_sync(0xFFFFFFFFu, (int)vec, 1) != 0 && lane > 0;
             if (act) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const bool head = i < 8 - a;  // stored by the previous lane's vector?
                     const bool done = head ? prev_vec : vec;
-                    if (!done && i >= lo && i < hi) out[y0 + i] = (uint16_t)r[i];
+                    if (!done && i >= lo && i < hi) {
+                        out[y0 + i] = (uint16_t)r[i];
+                        if (keep) win[y0 + i - w0] = (uint16_t)r[i];
+                    }
                 }
             }
         }
@@ -185,69 +215,82 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
                 if (x0 + i >= p0 && x0 + i < p1) out[x0 + i] = 0;
         }
     }
-    if (partials) {
-        const double s = block_sum_sq(sq, red);
+    if (keep) {
+        __syncthreads();   // the window is complete
+        const int64_t ng = V > 0 ? ((D + V + 7) >> 3) - (D >> 3) : 0;
+        const double s = tile_sumsq_cta<T>(win, ng, D - w0, D + V - w0, red);
         if (threadIdx.x == 0) partials[t] = s;
     }
 }
 
-// Recompute the per-tile partial sums from the reduced gradients, with
-// the chunks and the thread mapping of rs_kernel (8-element chunks aligned in
-// the source, chunk gi on thread gi mod THREADS, taken in increasing gi), so
-// the same bits.  A thread loads up to four of its chunks before it adds any
-// of them.  A whole chunk whose destination is off a 16-byte boundary is
-// read as the two aligned vectors around it and shifted: shard rows and
-// persistent space start and end on 8-element boundaries, so both vectors
-// lie in the chunk's row (they may cover a neighbouring tile's elements,
-// which are not used).
-constexpr int NORM_BATCH = 4;
+// Recompute the per-tile partial sums from the reduced gradients: one warp
+// per tile, persistent (warp w of the grid takes tiles w, w + warps, ...).
+// Lane c plays the virtual threads c, c+32, ..., c+224 of the tile norm in
+// that order, reading their groups of the tile's window straight from
+// global memory (16-byte loads, coalesced across the lanes), and adds their
+// pairs in column order; the butterfly across the lanes finishes the tile.
+// The groups of the next virtual thread are loaded before the current one
+// is summed.  The same function of the stored values as the reduce-scatter's
+// partials, so the same bits, with no shared memory and no block barrier.
+constexpr int NORM_CTAS_PER_SM = 4;
 
 template <class T>
-__global__ void __launch_bounds__(THREADS)
-norm_tiles_kernel(const ZsTile *__restrict__ tiles, const uint16_t *__restrict__ gs,
+__global__ void __launch_bounds__(THREADS, NORM_CTAS_PER_SM)
+norm_tiles_kernel(const ZsTile *__restrict__ tiles, int64_t ntiles, const uint16_t *__restrict__ gs,
                   const uint16_t *__restrict__ gP, double *__restrict__ partials) {
-    __shared__ SqRed red;
-    const int64_t t = blockIdx.x;
-    const ZsTile tile = tiles[t];
-    const uint16_t *__restrict__ in = tile.flat < 0 ? gP : gs;
-    const int64_t D = tile.dst, V = tile.valid;
-    const int64_t delta = tile.src - D;
-    const int64_t vs = tile.src, ve = tile.src + V;
-    const int64_t c_first = vs >> 3;
-    const int64_t nchunks = V > 0 ? ((ve - 1) >> 3) - c_first + 1 : 0;
-    SqAcc sq;
-    for (int64_t g0 = threadIdx.x; g0 < nchunks; g0 += NORM_BATCH * THREADS) {
-        uint4 v[NORM_BATCH];
-#pragma unroll
-        for (int u = 0; u < NORM_BATCH; ++u) {
-            const int64_t gi = g0 + (int64_t)u * THREADS;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (gi >= nchunks) continue;
-            const int64_t c = c_first + gi;
-            const int64_t lo = vs - 8 * c, hi = ve - 8 * c;
-            const int64_t y0 = 8 * c - delta;
-            if (lo <= 0 && hi >= 8) {
-                const int q = (int)(y0 & 7);
-                v[u] = ldg16(in + (y0 - q));
-                if (q) v[u] = shift8(v[u], ldg16(in + (y0 - q) + 8), q);
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * WARPS;
+    for (int64_t t = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5); t < ntiles; t += nw) {
+        const ZsTile tile = tiles[t];
+        const int64_t D = tile.dst, V = tile.valid;
+        const int64_t w0 = D & ~int64_t(7);
+        const uint16_t *__restrict__ win = (tile.flat < 0 ? gP : gs) + w0;
+        const int64_t ng = V > 0 ? ((D + V + 7) >> 3) - (D >> 3) : 0;
+        const int64_t lo = D - w0, hi = D + V - w0;
+        float ch = 0.0f, cl = 0.0f;
+        bool ok = true;
+        uint4 w[NORM_MAXG], nx[NORM_MAXG];
+        int n = vt_groups(win, lane, ng, lo, hi, w);
+#pragma unroll 1
+        for (int m = 0; m < NORM_VT / 32; ++m) {
+            int nn = 0;
+            if (m + 1 < NORM_VT / 32) nn = vt_groups(win, 32 * (m + 1) + lane, ng, lo, hi, nx);
+            const VtPair p = vt_sumsq<T>(w, n);
+            ok = ok && p.ok;
+            if (m == 0) {
+                ch = p.hi;
+                cl = p.lo;
             } else {
-                uint32_t r[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) r[i] = (i >= lo && i < hi) ? (uint32_t)in[y0 + i] : 0u;
-                v[u] = pack8(r);
+                add22(ch, cl, p.hi, p.lo);
             }
-        }
 #pragma unroll
-        for (int u = 0; u < NORM_BATCH; ++u) {
-            if (g0 + (int64_t)u * THREADS >= nchunks) continue;
-            uint32_t r[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) r[i] = lane16(v[u], i);
-            group_sq<T>(r, sq);
+            for (int j = 0; j < NORM_MAXG; ++j) w[j] = nx[j];
+            n = nn;
         }
+        double s;
+        if (__all_sync(0xFFFFFFFFu, ok)) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float h2 = __shfl_xor_sync(0xFFFFFFFFu, ch, off);
+                const float l2 = __shfl_xor_sync(0xFFFFFFFFu, cl, off);
+                add22(ch, cl, h2, l2);
+            }
+            s = __dadd_rn((double)ch, (double)cl);
+        } else {
+            // float64 for the whole tile, the same groups and tree
+            double c = 0.0;
+#pragma unroll 1
+            for (int m = 0; m < NORM_VT / 32; ++m) {
+                const int k = vt_groups(win, 32 * m + lane, ng, lo, hi, w);
+                const double f = vt_sumsq_f64<T>(w, k);
+                c = m == 0 ? f : __dadd_rn(c, f);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) c = __dadd_rn(c, __shfl_xor_sync(0xFFFFFFFFu, c, off));
+            s = c;
+        }
+        if (lane == 0) partials[t] = s;
     }
-    const double s = block_sum_sq(sq, red);
-    if (threadIdx.x == 0) partials[t] = s;
 }
 
 // First level: block c sums partials [c*CH, (c+1)*CH) in a fixed order.
@@ -329,19 +372,20 @@ static cudaError_t launch_rs_pdl(const ZsTile *d_tiles, int64_t tile0, int64_t n
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rs_kernel<FROM_TABLE, T, GROUPED>, d_tiles, tile0, p, tbl, N, G,
+    return cudaLaunchKernelEx(&cfg, rs_kernel<FROM_TABLE, T, GROUPED>, d_tiles, tile0, p, tbl, 0, N, G,
                               (float)N, gs, gP, partials);
 }
 
 template <class T>
 static cudaError_t launch_rs(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                             const RankPtrs &p, const void *const *d_table, int N, int G, uint16_t *gs,
+                             const RankPtrs &p, const void *const *d_table, int32_t bucket0, int N,
+                             int G, uint16_t *gs,
                              uint16_t *gP, double *partials, cudaStream_t s) {
     const auto *tbl = reinterpret_cast<const uint16_t *const *>(d_table);
     const dim3 g((unsigned)ntiles), b(THREADS);
     if (d_table) {
-        if (G == N) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
-        else rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, N, G, (float)N, gs, gP, partials);
+        if (G == N) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, bucket0, N, G, (float)N, gs, gP, partials);
+        else rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, bucket0, N, G, (float)N, gs, gP, partials);
         return cudaGetLastError();
     }
     const cudaError_t e =
@@ -357,18 +401,19 @@ cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t nti
     RankPtrs p;
     for (int k = 0; k < N; ++k) p.p[k] = static_cast<const uint16_t *>(rank_ptrs[k]);
     return dtype == ZS_DTYPE_FP16
-               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s)
-               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s);
+               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, nullptr, 0, N, G, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, nullptr, 0, N, G, gs, gP, partials, s);
 }
 
-cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t ntiles,
-                                   const void *const *d_table, int N, int G, int dtype, uint16_t *gs,
-                                   uint16_t *gP, double *partials, cudaStream_t s) {
+cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+                                   int32_t bucket0, const void *const *d_table, int N, int G,
+                                   int dtype, uint16_t *gs, uint16_t *gP, double *partials,
+                                   cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p = {};
     return dtype == ZS_DTYPE_FP16
-               ? launch_rs<FP16T>(d_tiles, 0, ntiles, p, d_table, N, G, gs, gP, partials, s)
-               : launch_rs<BF16T>(d_tiles, 0, ntiles, p, d_table, N, G, gs, gP, partials, s);
+               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, d_table, bucket0, N, G, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, d_table, bucket0, N, G, gs, gP, partials, s);
 }
 
 cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,
@@ -376,10 +421,28 @@ cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, in
                      float max_norm, float *d_norm, float *d_coef, int32_t *d_flags,
                      const ZsScaleArgs *scale, cudaStream_t s) {
     if (recompute && ntiles > 0) {
+        // persistent grid: NORM_CTAS_PER_SM CTAs on every SM (SM count per
+        // device, read once; atomic: host threads may launch at once)
+        static std::atomic<int> sms_of[64];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        int sms = sms_of[dev].load(std::memory_order_relaxed);
+        if (sms <= 0) {
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            if (sms <= 0) sms = 1;
+            sms_of[dev].store(sms, std::memory_order_relaxed);
+        }
+        const int64_t warps = (ntiles + WARPS - 1) / WARPS;
+        const int64_t grid = std::min<int64_t>(warps, (int64_t)sms * NORM_CTAS_PER_SM);
         if (dtype == ZS_DTYPE_FP16)
-            norm_tiles_kernel<FP16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, gs, gP, scratch);
+            norm_tiles_kernel<FP16T><<<(unsigned)grid, THREADS, 0, s>>>(d_tiles, ntiles, gs, gP,
+                                                                         scratch);
         else
-            norm_tiles_kernel<BF16T><<<(unsigned)ntiles, THREADS, 0, s>>>(d_tiles, gs, gP, scratch);
+            norm_tiles_kernel<BF16T><<<(unsigned)grid, THREADS, 0, s>>>(d_tiles, ntiles, gs, gP,
+                                                                         scratch);
     }
     norm_level1_kernel<<<(unsigned)n_level1, THREADS, 0, s>>>(scratch, ntiles, scratch + ntiles);
     ZsScaleArgs sc = {};
@@ -388,3 +451,4 @@ cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, in
                                              d_flags, sc);
     return cudaGetLastError();
 }
+
