@@ -229,8 +229,8 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
 // that order, reading their groups of the tile's window straight from
 // global memory (16-byte loads, coalesced across the lanes), and adds their
 // pairs in column order; the butterfly across the lanes finishes the tile.
-// The groups of the next virtual thread are loaded before the current one
-// is summed.  The same function of the stored values as the reduce-scatter's
+// On aligned tiles the groups of the next virtual thread are loaded before
+// the current one is summed.  The same function of the stored values as the reduce-scatter's
 // partials, so the same bits, with no shared memory and no block barrier.
 constexpr int NORM_CTAS_PER_SM = 4;
 
@@ -249,23 +249,52 @@ norm_tiles_kernel(const ZsTile *__restrict__ tiles, int64_t ntiles, const uint16
         const int64_t lo = D - w0, hi = D + V - w0;
         float ch = 0.0f, cl = 0.0f;
         bool ok = true;
-        uint4 w[NORM_MAXG], nx[NORM_MAXG];
-        int n = vt_groups(win, lane, ng, lo, hi, w);
-#pragma unroll 1
-        for (int m = 0; m < NORM_VT / 32; ++m) {
-            int nn = 0;
-            if (m + 1 < NORM_VT / 32) nn = vt_groups(win, 32 * (m + 1) + lane, ng, lo, hi, nx);
-            const VtPair p = vt_sumsq<T>(w, n);
-            ok = ok && p.ok;
-            if (m == 0) {
-                ch = p.hi;
-                cl = p.lo;
-            } else {
-                add22(ch, cl, p.hi, p.lo);
-            }
+        uint4 w[NORM_MAXG];
+        if (((D | V) & 7) == 0 && ng <= 4 * NORM_VT) {
+            // aligned tile (every Llama-shaped tile): the window is the values,
+            // at most 4 groups per virtual thread, no masking; the groups of
+            // the next virtual thread are in flight while one is summed
+            uint4 q[2][4];
+            int nq[2];
+            auto load = [&](int m, uint4 (&o)[4]) {
+                int c = 0;
 #pragma unroll
-            for (int j = 0; j < NORM_MAXG; ++j) w[j] = nx[j];
-            n = nn;
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t g = 32 * m + lane + (int64_t)NORM_VT * j;
+                    o[j] = make_uint4(0, 0, 0, 0);
+                    if (g < ng) {
+                        o[j] = *reinterpret_cast<const uint4 *>(win + 8 * g);
+                        c = j + 1;
+                    }
+                }
+                return c;
+            };
+            nq[0] = load(0, q[0]);
+#pragma unroll
+            for (int m = 0; m < NORM_VT / 32; ++m) {
+                if (m + 1 < NORM_VT / 32) nq[(m + 1) & 1] = load(m + 1, q[(m + 1) & 1]);
+                const VtPair p = vt_sumsq<T>(q[m & 1], nq[m & 1]);
+                ok = ok && p.ok;
+                if (m == 0) {
+                    ch = p.hi;
+                    cl = p.lo;
+                } else {
+                    add22(ch, cl, p.hi, p.lo);
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int m = 0; m < NORM_VT / 32; ++m) {
+                const int n = vt_groups(win, 32 * m + lane, ng, lo, hi, w);
+                const VtPair p = vt_sumsq<T>(w, n);
+                ok = ok && p.ok;
+                if (m == 0) {
+                    ch = p.hi;
+                    cl = p.lo;
+                } else {
+                    add22(ch, cl, p.hi, p.lo);
+                }
+            }
         }
         double s;
         if (__all_sync(0xFFFFFFFFu, ok)) {
