@@ -147,6 +147,12 @@ gather_bulk_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t
     // stages' mbarriers
     extern __shared__ __align__(128) uint8_t stage[];
     if (threadIdx.x != 0) return;
+    // Launched as a programmatic dependent: wait until the previous kernel
+    // of the stream has finished and its writes (the parameter shards) are
+    // visible, then let the next gather start placing its CTAs, which wait
+    // the same way; back-to-back gathers then lose the launch gap.
+    asm volatile("griddepcontrol.wait;" : : : "memory");
+    asm volatile("griddepcontrol.launch_dependents;" : : : "memory");
     const uint32_t base = smem_u32(stage);
     if (base & 15) {                     // bulk copies need 16-byte aligned buffers
         atomicAdd(&g_bulk_wait_timeouts, 1);
@@ -269,8 +275,18 @@ cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *
         const int64_t chunks = (a.out_hi - a.out_lo + BULK_CHUNK_ELEMS - 1) / BULK_CHUNK_ELEMS;
         const int64_t cap = max_ctas > 0 ? max_ctas : wave;
         const int64_t blocks = chunks < cap ? chunks : cap;
-        gather_bulk_kernel<<<(unsigned)blocks, 32, BULK_SMEM_ALLOC, s>>>(a, shards, flat_out);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(32);
+        cfg.dynamicSmemBytes = BULK_SMEM_ALLOC;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gather_bulk_kernel, a, shards, flat_out);
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     const int a0 = (int)((reinterpret_cast<uintptr_t>(flat_out) >> 1) & 7);
     const int64_t groups = ((a0 + a.out_hi - 1) >> 3) - ((a0 + a.out_lo) >> 3) + 1;
