@@ -85,3 +85,29 @@ def test_group_equal_to_n_is_zero3():
     for k in xa:
         assert np.array_equal(xa[k].view(np.uint8), xb[k].view(np.uint8)), k
     assert np.array_equal(a.flat.u16(), b.flat.u16())
+
+
+def test_hsdp_ranges_equal_per_bucket(case):
+    """zs_reduce_scatter_range over random runs of buckets gives the
+    per-bucket calls' bits (grouped sums, fp16 included), and the same norm
+    partials."""
+    import zero_sharded_optimizer_bucket_gb300 as zs
+    a, b = H.DevicePlan(**CASES[case]), H.DevicePlan(**CASES[case])
+    for d in (a, b):
+        d.init_weights()
+        d.set_grads(500, use_gpu_generator=case.startswith("many"))
+    a.reduce_scatter_all_buckets(with_scratch=True)
+    nb = len(b.op.reduce_buckets)
+    rng = np.random.default_rng(nb + 1)
+    cuts = sorted({0, nb, *[int(x) for x in rng.integers(0, nb + 1, size=min(nb, 4))]})
+    for lo, hi in zip(cuts[:-1], cuts[1:]):
+        zs.zs_reduce_scatter_range(b.plan, lo, hi - lo, b.ptr_table[lo * b.N:],
+                                   b.bufs["grad_shards"].ptr(), b.bufs["persist_grads"].ptr(),
+                                   b.scratch.ptr())
+    xa, xb = a.snapshot(), b.snapshot()
+    for k in ("grad_shards", "persist_grads"):
+        assert np.array_equal(xa[k], xb[k]), k
+    for d in (a, b):
+        d.grad_norm(1.0, recompute=False)
+    assert H.same_bits(a.d_norm.np()[0], b.d_norm.np()[0])
+    b.check_canaries()
