@@ -216,11 +216,7 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         }
     }
     if (keep) {
-        // Aligned in the source and the destination, chunk gi is window
-        // group gi: each thread wrote exactly its own virtual thread's groups
-        // and reads them back itself.  Otherwise the other threads' writes
-        // must be complete.
-        if (a != 0 || (D & 7) != 0) __syncthreads();
+        __syncthreads();   // the window is complete
         const int64_t ng = V > 0 ? ((D + V + 7) >> 3) - (D >> 3) : 0;
         const double s = tile_sumsq_cta<T>(win, ng, D - w0, D + V - w0, red);
         if (threadIdx.x == 0) partials[t] = s;
