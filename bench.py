@@ -111,12 +111,12 @@ class DeviceWorkload:
         # gradient pool
         nb = info["n_reduce_buckets"]
         self.buf_elems = [zs.zs_bucket_info(self.plan, b)["buf_elems"] for b in range(nb)]
-        total = sum(N * _align8(L) for L in self.buf_elems)
+        total = sum(N * wl.pool_align(L) for L in self.buf_elems)
         if pool_elems is None:
             free = torch.cuda.mem_get_info(self.dev)[0]
             cap = max((free - (6 << 30)) // 2, 0)
             pool_elems = min(total, cap)
-        need = (N + 1) * _align8(max(self.buf_elems, default=8))
+        need = (N + 1) * wl.pool_align(max(self.buf_elems, default=8))
         pool_elems = max(int(pool_elems), min(need, total) if total else 8)
         if total and pool_elems < total:
             pool_elems = max(pool_elems, need)
@@ -482,8 +482,8 @@ def _oracle_part(spec):
     W = philox.weight_f32(spec["seed"], spec["w_off"] + np.arange(n_w, dtype=np.uint64),
                           spec["weight_sigma"])
     st = ostep.partition(plan, np.resize(W, plan.input_elems))
-    need = sum(plan.n_ranks * ((L + 7) // 8 * 8) for L in plan.bucket_buf_elems)
-    largest = (max(plan.bucket_buf_elems, default=8) + 7) // 8 * 8
+    need = sum(plan.n_ranks * wl.pool_align(L) for L in plan.bucket_buf_elems)
+    largest = wl.pool_align(max(plan.bucket_buf_elems, default=8))
     M = max(8, min(need, max(P, (plan.n_ranks + 1) * largest)))
     idx = spec["g_off"] + np.arange(min(M, P), dtype=np.uint64)
     if spec["dtype"] == "fp16":
@@ -691,7 +691,7 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
     N, nb = dw.N, len(dw.buf_elems)
     if nb == 0:
         return None
-    sizes = [N * _align8(L) for L in dw.buf_elems]
+    sizes = [N * wl.pool_align(L) for L in dw.buf_elems]
     total = sum(sizes)
     H = min(total, max(host_pool_bytes // 2, 2 * max(sizes)))
     host = torch.empty(H, dtype=torch.int16, pin_memory=True)
@@ -723,7 +723,7 @@ def run_e2e(dw, steps=2, warmup=1, host_pool_bytes=4 << 30, slots=4):
                 filled[s].record(cs)
             comp.wait_event(filled[s])
             base = ring.data_ptr() + 2 * s * smax
-            ptrs = [base + 2 * k * _align8(dw.buf_elems[b]) for k in range(N)]
+            ptrs = [base + 2 * k * wl.pool_align(dw.buf_elems[b]) for k in range(N)]
             zs.zs_reduce_scatter(dw.plan, b, ptrs, dw.gs, dw.gP, dw.scratch)
             free[s].record(comp)
             used[s] = True

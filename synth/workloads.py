@@ -218,20 +218,30 @@ WORKLOADS = {
 }
 
 
+POOL_ALIGN = 64      # elements: every buffer starts on a 128-byte boundary
+
+
+def pool_align(n: int) -> int:
+    """n rounded up to the pool's buffer alignment (64 elements, 128 bytes,
+    as separately allocated buffers are aligned at least)."""
+    return (int(n) + POOL_ALIGN - 1) // POOL_ALIGN * POOL_ALIGN
+
+
 def pool_offsets(bucket_buf_elems, n_ranks: int, pool_elems: int):
     """Element offsets into a gradient pool for every (bucket, rank) buffer.
 
     Bucket b of rank k reads `pool[off[b][k] : off[b][k] + bucket_buf_elems[b]]`.
-    Buffers are laid one after another (8-element aligned); when the pool is
-    exhausted the layout restarts at 0, so a pool smaller than the whole
-    step's gradients is reused with a reuse distance of the full pool.
+    Buffers are laid one after another, each starting on a 128-byte
+    boundary; when the pool is exhausted the layout restarts at 0, so a pool
+    smaller than the whole step's gradients is reused with a reuse distance
+    of the full pool.
     """
     offs = []
     run = 0
-    total = sum((int(L) + 7) // 8 * 8 for L in bucket_buf_elems) * n_ranks
+    total = sum(pool_align(L) for L in bucket_buf_elems) * n_ranks
     wraps = total > pool_elems
     for L in bucket_buf_elems:
-        L8 = (int(L) + 7) // 8 * 8
+        L8 = pool_align(L)
         if wraps and L8 * (n_ranks + 1) > pool_elems:
             # (N+1) buffers guarantee that the buffers of one bucket never
             # overlap when the layout wraps around in the middle of a bucket

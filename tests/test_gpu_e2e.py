@@ -24,7 +24,7 @@ def test_e2e_leg_equals_fused_steps():
     a = bench.DeviceWorkload(w, "cuda:0")
     b = bench.DeviceWorkload(w, "cuda:0")
     try:
-        total = sum(a.N * bench._align8(L) for L in a.buf_elems)
+        total = sum(a.N * workloads.pool_align(L) for L in a.buf_elems)
         assert a.pool_elems >= total     # no wrap: the host buffer holds the same gradients
         r = bench.run_e2e(a, steps=2, warmup=1)
         for _ in range(3):

@@ -43,14 +43,14 @@ def test_workload_sizes():
 
 def test_pool_offsets_disjoint_within_bucket():
     offs = workloads.pool_offsets([100, 1000, 37, 5000], 4, 30_000)
-    lens = [104, 1000, 40, 5000]
+    lens = [128, 1024, 64, 5056]
     for row, L in zip(offs, lens):
         spans = sorted((o, o + L) for o in row)
         for (a, b), (c, d) in zip(spans, spans[1:]):
             assert b <= c
-        assert all(o % 8 == 0 and o + L <= 30_000 for o in row)
+        assert all(o % 64 == 0 and o + L <= 30_000 for o in row)
 
 
 def test_pool_offsets_exact_fit_without_wrap():
-    offs = workloads.pool_offsets([40], 4, 160)
-    assert offs == [[0, 40, 80, 120]]
+    offs = workloads.pool_offsets([40], 4, 256)
+    assert offs == [[0, 64, 128, 192]]

@@ -89,11 +89,18 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     // the norm partial is formed from a shared-memory copy of the results
     const bool keep = partials != nullptr;
     const int64_t w0 = D & ~int64_t(7);
+    // Chunks are numbered from c0, the tile's first chunk rounded down to a
+    // multiple of 8: a warp's 32 chunks then start on a 128-byte boundary of
+    // every rank buffer whose start is 128-byte aligned, so a warp's load of
+    // one rank touches exactly four lines instead of five.  Lanes before the
+    // tile's first chunk only take part in the shuffles.
+    const int64_t c0 = c_first & ~int64_t(7);
+    const int64_t nspan = nchunks > 0 ? c_first - c0 + nchunks : 0;
     // uniform trip count: every lane takes part in the shuffles
-    for (int64_t base = 0; base < nchunks; base += THREADS) {
+    for (int64_t base = 0; base < nspan; base += THREADS) {
         const int64_t gi = base + threadIdx.x;
-        const bool act = gi < nchunks;
-        const int64_t c = c_first + gi;
+        const int64_t c = c0 + gi;
+        const bool act = c >= c_first && gi < nspan;
         const int64_t lo = vs - 8 * c, hi = ve - 8 * c;  // valid lanes [lo, hi)
         float acc[8];
 #pragma unroll
