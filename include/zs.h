@@ -278,11 +278,15 @@ zs_status zs_partition(const zs_plan *plan, const float *full_params, const zs_s
  * that order (0 for e >= numel); grad_shards[r][S_p+j] = bf16_rne(s / N).
  * Persistent entries write persist_grads the same way on the full range.
  * rank_grads: HOST array of N device pointers (16-byte aligned, >=
- * buf_elems elements each).  If norm_scratch is not NULL (>=
- * norm_scratch_elems doubles), the bucket's tiles also write their sums of
- * squared results there for zs_grad_norm.  Errors: ZS_EINVAL (bucket out
- * of range, N > ZS_MAX_RANKS, NULL or misaligned pointer), ZS_ESTATE,
- * ZS_ECUDA. */
+ * buf_elems elements each; buffers that start on 128-byte boundaries, as
+ * separate allocations do, are read a line at a time).  If norm_scratch is
+ * not NULL (>= norm_scratch_elems doubles), the bucket's tiles also write
+ * their sums of squared results there for zs_grad_norm.  The launch keeps
+ * stream order: it waits for the previous kernel of the stream before
+ * reading, so back-to-back calls each leave the GPU partly idle while the
+ * previous bucket drains; zs_reduce_scatter_range takes several ready
+ * buckets in one launch.  Errors: ZS_EINVAL (bucket out of range,
+ * N > ZS_MAX_RANKS, NULL or misaligned pointer), ZS_ESTATE, ZS_ECUDA. */
 zs_status zs_reduce_scatter(const zs_plan *plan, int32_t bucket, const void *const *rank_grads,
                             void *grad_shards, void *persist_grads, double *norm_scratch,
                             void *stream);
