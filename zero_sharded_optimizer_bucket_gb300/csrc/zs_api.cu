@@ -197,7 +197,8 @@ zs_status zs_adam_step(const zs_plan *P, int32_t sub_group, const zs_adam_hparam
 
 zs_status zs_gather_impl(const zs_plan *P, int32_t n, const int32_t *params,
                          const void *param_shards, void *flat_out, int64_t flat_capacity,
-                         int64_t *view_offsets, void *stream, int max_ctas, const char *fn) {
+                         int64_t *view_offsets, void *stream, int max_ctas, bool dependent,
+                         const char *fn) {
     zs_status r = need_table(P, fn);
     if (r) return r;
     if (n < 0 || (n > 0 && (!params || !view_offsets)))
@@ -242,7 +243,7 @@ zs_status zs_gather_impl(const zs_plan *P, int32_t n, const int32_t *params,
         if (a.n == 0) return ZS_OK;
         const cudaError_t e = zsl_gather(a, static_cast<const uint16_t *>(param_shards),
                                          static_cast<uint16_t *>(flat_out), (cudaStream_t)stream,
-                                         max_ctas);
+                                         max_ctas, dependent);
         a.n = 0;
         return cuda_status(e, fn);
     };
@@ -288,7 +289,7 @@ zs_status zs_all_gather_coalesced(const zs_plan *P, int32_t n, const int32_t *pa
                                   const void *param_shards, void *flat_out,
                                   int64_t flat_capacity, int64_t *view_offsets, void *stream) {
     return zs_gather_impl(P, n, params, param_shards, flat_out, flat_capacity, view_offsets,
-                          stream, 0, "zs_all_gather_coalesced");
+                          stream, 0, true, "zs_all_gather_coalesced");
 }
 
 zs_status zs_unscale_and_clip(const zs_plan *P, const void *grad_shards, const void *persist_grads,

@@ -147,10 +147,11 @@ gather_bulk_kernel(ZsGatherArgs a, const uint16_t *__restrict__ shards, uint16_t
     // stages' mbarriers
     extern __shared__ __align__(128) uint8_t stage[];
     if (threadIdx.x != 0) return;
-    // Launched as a programmatic dependent: wait until the previous kernel
-    // of the stream has finished and its writes (the parameter shards) are
-    // visible, then let the next gather start placing its CTAs, which wait
-    // the same way; back-to-back gathers then lose the launch gap.
+    // When launched as a programmatic dependent: wait until the previous
+    // kernel of the stream has finished and its writes (the parameter
+    // shards) are visible, then let the next gather start placing its CTAs,
+    // which wait the same way; back-to-back gathers then lose the launch
+    // gap.  In an ordinary launch both instructions have no effect.
     asm volatile("griddepcontrol.wait;" : : : "memory");
     asm volatile("griddepcontrol.launch_dependents;" : : : "memory");
     const uint32_t base = smem_u32(stage);
@@ -247,7 +248,7 @@ bool bulk_ok(const ZsGatherArgs &a, const uint16_t *shards, const uint16_t *flat
 }  // namespace
 
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
-                       cudaStream_t s, int max_ctas) {
+                       cudaStream_t s, int max_ctas, bool dependent) {
     if (a.n <= 0 || a.out_hi <= a.out_lo) return cudaSuccess;
     if (bulk_ok(a, shards, flat_out)) {
         // per device: its SM count, and the kernel's shared-memory opt-in
@@ -284,7 +285,7 @@ cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = dependent ? 1 : 0;
         e = cudaLaunchKernelEx(&cfg, gather_bulk_kernel, a, shards, flat_out);
         return e != cudaSuccess ? e : cudaGetLastError();
     }

@@ -77,7 +77,10 @@ zs_status zs_fail(zs_status status, const char *fmt, ...)
 void zs_clear_error();
 
 // zs_all_gather_coalesced with its grid capped at max_ctas CTAs (0: no cap
-// beyond the default); fn names the caller in error messages.
+// beyond the default); dependent: bulk-path launches are programmatic
+// dependents of the previous kernel of the stream; fn names the caller in
+// error messages.
 zs_status zs_gather_impl(const zs_plan *P, int32_t n, const int32_t *params,
                          const void *param_shards, void *flat_out, int64_t flat_capacity,
-                         int64_t *view_offsets, void *stream, int max_ctas, const char *fn);
+                         int64_t *view_offsets, void *stream, int max_ctas, bool dependent,
+                         const char *fn);

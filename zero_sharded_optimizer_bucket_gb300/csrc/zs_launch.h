@@ -64,8 +64,12 @@ struct ZsGatherArgs {
 };
 
 // max_ctas caps the grid (0: the default, 8 CTAs per SM on either path)
+// dependent: bulk-path launches are programmatic dependents of the previous
+// kernel of the stream (back-to-back gathers lose the launch gap; the
+// waiting CTAs hold their shared memory, so gathers that run beside other
+// work are launched plainly)
 cudaError_t zsl_gather(const ZsGatherArgs &a, const uint16_t *shards, uint16_t *flat_out,
-                       cudaStream_t s, int max_ctas);
+                       cudaStream_t s, int max_ctas, bool dependent);
 // Number of bounded waits of the bulk gather that gave up (synchronous).
 cudaError_t zsl_bulk_wait_timeouts(int *count, bool reset);
 // One bounded wait on an mbarrier nothing arrives on (gives up after limit_ns).

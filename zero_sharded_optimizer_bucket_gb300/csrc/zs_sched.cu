@@ -185,7 +185,8 @@ zs_status gather(zs_sched *s, std::vector<int32_t> params, int64_t pos, const vo
     }
     std::vector<int64_t> views(params.size());
     r = zs_gather_impl(s->P, (int32_t)params.size(), params.data(), shards, s->arena + offs[0],
-                       block, views.data(), gstream, (int)s->cfg.gather_ctas, "zs_sched_fetch");
+                       block, views.data(), gstream, (int)s->cfg.gather_ctas, false,
+                       "zs_sched_fetch");
     if (r) return r;
     for (size_t i = 0; i < params.size(); ++i)
         if (views[i] != offs[i] - offs[0])
