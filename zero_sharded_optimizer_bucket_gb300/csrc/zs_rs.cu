@@ -33,20 +33,36 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     // the tile's results in destination order (the window of the tile norm)
     __shared__ __align__(16) uint16_t win[NORM_WIN_ELEMS];
     const int64_t t = tile0 + blockIdx.x;
-    if (!FROM_TABLE && threadIdx.x == 0) {
-        // a per-bucket launch is a programmatic dependent: fetch the tile
-        // descriptor (the plan's table, which no kernel writes) into L1
-        // while the previous kernel finishes
-        const char *d = reinterpret_cast<const char *>(tiles + t);
-        asm volatile("prefetch.global.L1 [%0];" : : "l"(d));
-        asm volatile("prefetch.global.L1 [%0];" : : "l"(d + sizeof(ZsTile) - 1));
+    // the plan's tile table: written by copies only, never by a kernel, so
+    // it may be read before the wait below
+    const ZsTile tile = tiles[t];
+    if (!FROM_TABLE && tile.valid > 0 && threadIdx.x < N) {
+        // A per-bucket launch is a programmatic dependent whose CTAs can be
+        // placed while the previous kernel drains.  Meanwhile each of them
+        // has the chunks that its first pass of the loop below reads (the
+        // 256 chunks from the line-aligned first chunk, clipped to the
+        // tile) fetched into L2, one bulk prefetch per rank.  A prefetch
+        // changes no value any load can see: the L2 is the GPU's point of
+        // coherence, and the loads still come after the wait.  Fetching
+        // the whole tile instead measured slower: the extra requests
+        // compete with the loads of the CTAs that start after the wait.
+        const uint16_t *q = ptrs.p[threadIdx.x];
+        if (q != nullptr && !(reinterpret_cast<uintptr_t>(q) & 15u)) {
+            const int64_t lo = tile.src & ~int64_t(7);
+            const int64_t first = ((tile.src >> 3) & ~int64_t(7)) * 8;
+            const int64_t hi =
+                min((tile.src + tile.valid + 7) & ~int64_t(7), first + 8 * int64_t(THREADS));
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         :
+                         : "l"(__cvta_generic_to_global(q + lo)), "r"((uint32_t)(2 * (hi - lo)))
+                         : "memory");
+        }
     }
     // Wait until the previous kernel of the stream has finished and its
     // writes are visible (a no-op in an ordinary launch), then let the next
     // dependent launch start placing its CTAs, which wait the same way.
     asm volatile("griddepcontrol.wait;" : : : "memory");
     asm volatile("griddepcontrol.launch_dependents;" : : : "memory");
-    const ZsTile tile = tiles[t];
     // stage the rank pointers; one barrier, with a per-warp vote on their use
     int my_bad = 0;
     for (int k = threadIdx.x; k < N; k += THREADS) {
