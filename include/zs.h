@@ -250,7 +250,12 @@ zs_status zs_sub_group_info(const zs_plan *plan, int32_t sub_group, zs_sub_group
  * element `src` on of the bucket `bucket`'s gradient buffers and from
  * element `win` on of input space; the rest are zero padding; its first
  * flat_len elements also go to model flat space from element `flat` on.
- * Errors: ZS_EINVAL (bytes < device_table_bytes). */
+ * When bytes >= device_table_bytes the rest of the device table follows:
+ * n_tiles int32, the launch order of zs_reduce_scatter (launch position
+ * i, in tile numbering, works on tile order[i]; within each bucket a
+ * permutation of the bucket's tiles, most valid elements first, then
+ * longest, then table order, so that a bucket's launch does not end on a
+ * large tile that started late).  Errors: ZS_EINVAL (bytes < 48 * n_tiles). */
 zs_status zs_plan_table(const zs_plan *plan, void *host_out, int64_t bytes);
 
 /* Copy the plan's work tables to device memory owned by the caller

@@ -141,11 +141,27 @@ def test_llama3_8b_plan_shape():
     assert info["psi"] == 8_030_261_248
 
 
+def _check_launch_order(cp, t):
+    """The reduce-scatter's launch order: within each bucket a permutation
+    of the bucket's tiles, most valid elements first, then longest, then
+    table order."""
+    order = zs.zs_plan_launch_order(cp)
+    assert order.size == len(t)
+    for b in range(zs.zs_plan_info(cp)["n_reduce_buckets"]):
+        bi = zs.zs_bucket_info(cp, b)
+        f, n = bi["first_tile"], bi["n_tiles"]
+        o = order[f:f + n].astype(np.int64)
+        assert sorted(o.tolist()) == list(range(f, f + n)), b
+        key = [(-int(t[i]["valid"]), -int(t[i]["len"]), int(i)) for i in o]
+        assert key == sorted(key), b
+
+
 def _check_tiles(op, cp):
     """Tiles cover every shard-space and persistent-space element exactly
     once, and each valid element maps to the bucket position and input
     position the oracle's definitions give."""
     t = zs.zs_plan_table(cp)
+    _check_launch_order(cp, t)
     N, S = op.group, op.S
     cover = np.zeros(N * S, dtype=np.int32)
     pcover = np.zeros(op.Pn_alloc, dtype=np.int32)

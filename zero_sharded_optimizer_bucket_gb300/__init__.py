@@ -327,6 +327,19 @@ def zs_plan_table(plan):
     return arr
 
 
+def zs_plan_launch_order(plan):
+    """The reduce-scatter's launch order (int32 per tile: launch position i
+    works on tile order[i]), the part of the device table after the tiles."""
+    import numpy as np
+    info = zs_plan_info(plan)
+    n = info["n_tiles"]
+    buf = np.zeros(info["device_table_bytes"], dtype=np.uint8)
+    _check(_lib.zs_plan_table(_h(plan), buf.ctypes.data if buf.size else None, buf.nbytes),
+           "zs_plan_table")
+    rec = np.dtype(TILE_DTYPE).itemsize
+    return buf[rec * n:(rec + 4) * n].view(np.int32).copy()
+
+
 def zs_plan_upload(plan, d_table, nbytes: int, stream=None) -> None:
     _check(_lib.zs_plan_upload(_h(plan), _ptr(d_table), int(nbytes), _stream(stream)),
            "zs_plan_upload")

@@ -93,9 +93,11 @@ extern "C" {
 
 zs_status zs_plan_upload(zs_plan *P, void *d_table, int64_t bytes, void *stream) {
     if (!P) return zs_fail(ZS_EINVAL, "zs_plan_upload: NULL plan");
-    const int64_t need = (int64_t)(P->tiles.size() * sizeof(ZsTile));
-    if (need == 0) {
+    const int64_t ntiles = (int64_t)P->tiles.size();
+    const int64_t need = zs_table_bytes(ntiles), tile_bytes = zs_table_tile_bytes(ntiles);
+    if (ntiles == 0) {
         P->d_tiles = static_cast<const ZsTile *>(d_table);
+        P->d_rs_order = nullptr;
         zs_clear_error();
         return ZS_OK;
     }
@@ -103,10 +105,15 @@ zs_status zs_plan_upload(zs_plan *P, void *d_table, int64_t bytes, void *stream)
     if (bytes < need)
         return zs_fail(ZS_EINVAL, "zs_plan_upload: %lld bytes < %lld needed", (long long)bytes,
                        (long long)need);
-    const cudaError_t e = cudaMemcpyAsync(d_table, P->tiles.data(), (size_t)need,
-                                          cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    char *d = static_cast<char *>(d_table);
+    cudaError_t e = cudaMemcpyAsync(d, P->tiles.data(), (size_t)tile_bytes,
+                                    cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d + tile_bytes, P->rs_order.data(), (size_t)ntiles * 4,
+                            cudaMemcpyHostToDevice, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_status(e, "zs_plan_upload: cudaMemcpyAsync");
     P->d_tiles = static_cast<const ZsTile *>(d_table);
+    P->d_rs_order = reinterpret_cast<const int32_t *>(d + tile_bytes);
     zs_clear_error();
     return ZS_OK;
 }
@@ -143,7 +150,7 @@ zs_status zs_reduce_scatter(const zs_plan *P, int32_t bucket, const void *const 
     if (norm_scratch && !al(norm_scratch, 8))
         return zs_fail(ZS_EINVAL, "%s: norm_scratch not 8-byte aligned", fn);
     const ZsBucket &b = P->buckets[bucket];
-    return cuda_status(zsl_reduce_scatter(P->d_tiles, b.first_tile, b.n_tiles, rank_grads, N, P->G,
+    return cuda_status(zsl_reduce_scatter(P->d_tiles, P->d_rs_order, b.first_tile, b.n_tiles, rank_grads, N, P->G,
                                           P->cfg.dtype,
                                           static_cast<uint16_t *>(grad_shards),
                                           static_cast<uint16_t *>(persist_grads), norm_scratch,

@@ -26,6 +26,13 @@ static_assert(sizeof(ZsTile) == 48, "tile layout");
 constexpr int64_t ZS_TILE_ELEMS = 8192;     // destination elements per tile (before alignment)
 constexpr int64_t ZS_LEVEL1_CHUNK = 4096;   // tile partial sums per first-level norm block
 
+// Bytes of the device table: the tile records, then the reduce-scatter's
+// launch order (int32 per tile), padded to 16 bytes.
+inline int64_t zs_table_tile_bytes(int64_t ntiles) { return ntiles * (int64_t)sizeof(ZsTile); }
+inline int64_t zs_table_bytes(int64_t ntiles) {
+    return zs_table_tile_bytes(ntiles) + (ntiles * 4 + 15) / 16 * 16;
+}
+
 struct ZsParam {
     int64_t numel, ds_id, ps, pad;
     int64_t shard_off, persist_off, flat_off, input_off;
@@ -62,10 +69,17 @@ struct zs_plan {
     std::vector<ZsGather> gathers;
     std::vector<ZsSubGroup> sub_groups;
     std::vector<ZsTile> tiles;
+    // launch order of the per-bucket reduce-scatter: launch position i
+    // (numbered like the tiles) works on tile rs_order[i].  Within each
+    // bucket the tiles go largest first, so that a launch does not end
+    // waiting on one large tile that started late; no result depends on
+    // this order.
+    std::vector<int32_t> rs_order;
     int64_t S = 0, S_logical = 0, Pn_alloc = 0, Pn = 0, psi = 0, flat_elems = 0;
     int64_t padding = 0, max_buf = 0, max_gather = 0, n_level1 = 1;
     int32_t G = 1;                     // shard owners per group (N unless HSDP)
     const ZsTile *d_tiles = nullptr;   // caller memory given to zs_plan_upload
+    const int32_t *d_rs_order = nullptr;   // rs_order, after the tiles in that memory
 };
 
 // Records a message for zs_last_error() and returns status.

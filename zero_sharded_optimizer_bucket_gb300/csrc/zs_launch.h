@@ -20,8 +20,10 @@ struct ZsScaleArgs {
     int32_t window;
 };
 
-cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                               const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
+// One bucket: launch positions [tile0, tile0 + ntiles); position i works on
+// tile d_order[i] (the plan's per-bucket largest-first permutation).
+cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, const int32_t *d_order, int64_t tile0,
+                               int64_t ntiles, const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
                                uint16_t *gP, double *partials, cudaStream_t s);
 
 // Tiles [tile0, tile0 + ntiles) (whole buckets from bucket0 on); rank k's

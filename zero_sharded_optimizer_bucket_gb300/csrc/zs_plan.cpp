@@ -177,6 +177,20 @@ zs_status build(zs_plan &P, int32_t n, const int64_t *numel, const int64_t *ds_i
         bk.n_tiles = (int64_t)P.tiles.size() - bk.first_tile;
         P.max_buf = std::max(P.max_buf, bk.buf_elems);
     }
+    if (P.tiles.size() > (size_t)INT32_MAX)
+        return zs_fail(ZS_EINVAL, "zs_build_partition: %zu work tiles exceed the int32 launch order",
+                       P.tiles.size());
+    // the reduce-scatter's launch order: per bucket, most valid elements
+    // first (then longest, then table order)
+    P.rs_order.resize(P.tiles.size());
+    for (const ZsBucket &bk : P.buckets) {
+        int32_t *o = P.rs_order.data() + bk.first_tile;
+        for (int64_t i = 0; i < bk.n_tiles; ++i) o[i] = (int32_t)(bk.first_tile + i);
+        std::stable_sort(o, o + bk.n_tiles, [&P](int32_t a, int32_t b) {
+            const ZsTile &x = P.tiles[a], &y = P.tiles[b];
+            return x.valid != y.valid ? x.valid > y.valid : x.len > y.len;
+        });
+    }
 
     // gather buckets
     const int64_t G = c.prefetch_bucket_size;
@@ -323,7 +337,7 @@ zs_status zs_plan_info(const zs_plan *P, zs_plan_info_t *o) {
     o->max_gather_elems = P->max_gather;
     o->bytes_per_rank = 16 * (P->S_logical + P->Pn);
     o->n_tiles = (int64_t)P->tiles.size();
-    o->device_table_bytes = (int64_t)(P->tiles.size() * sizeof(ZsTile));
+    o->device_table_bytes = zs_table_bytes((int64_t)P->tiles.size());
     o->norm_scratch_elems = (int64_t)P->tiles.size() + P->n_level1;
     return ZS_OK;
 }
@@ -421,10 +435,13 @@ zs_status zs_sub_group_info(const zs_plan *P, int32_t s, zs_sub_group_info_t *o)
 
 zs_status zs_plan_table(const zs_plan *P, void *host_out, int64_t bytes) {
     if (!P || (!host_out && bytes > 0)) return zs_fail(ZS_EINVAL, "zs_plan_table: NULL argument");
-    const int64_t need = (int64_t)(P->tiles.size() * sizeof(ZsTile));
+    const int64_t n = (int64_t)P->tiles.size();
+    const int64_t need = zs_table_tile_bytes(n);
     if (bytes < need) return zs_fail(ZS_EINVAL, "zs_plan_table: %lld bytes < %lld", (long long)bytes,
                                      (long long)need);
     if (need) std::memcpy(host_out, P->tiles.data(), (size_t)need);
+    if (n && bytes >= zs_table_bytes(n))
+        std::memcpy(static_cast<char *>(host_out) + need, P->rs_order.data(), (size_t)n * 4);
     return ZS_OK;
 }
 

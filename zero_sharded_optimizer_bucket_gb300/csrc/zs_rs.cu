@@ -1,7 +1,7 @@
 // A2 reduce-scatter (with the A3 partial sums) and the A3 norm kernels.
 //
 // Reduce-scatter ([ZeRO-3 chapter] §6.2, avg-scatter of a full bucket):
-// one CTA per tile.  A thread owns 8-element chunks aligned to 16 bytes in
+// one CTA per tile, a bucket's tiles launched largest first.  A thread owns 8-element chunks aligned to 16 bytes in
 // the rank buffers; for each rank k in order 0..N-1 it loads the chunk of
 // rank k's bucket buffer with one 16-byte load, adds the 8 values to 8
 // float32 sums, then writes bf16_rne(sum / N) to the owners' shard slots
@@ -22,9 +22,20 @@ struct RankPtrs {
     const uint16_t *p[ZS_MAX_RANKS];
 };
 
+constexpr int RS_CTAS_PER_SM = 5;
+
+// FROM_TABLE: one launch over whole buckets (the fused step, a range of
+// buckets), rank pointers from a device table, launch position i on tile i.
+// Otherwise one bucket: rank pointers in the arguments, launch position i
+// on tile order[i] (the bucket's tiles largest first, so that the launch
+// does not end on a large tile that started late; in a launch over many
+// buckets the tail comes once and the plain order, which mixes large and
+// small tiles, keeps the CTA launch rate from mattering), and with
+// prefetch != 0 the first pass fetched into L2 before the dependent wait.
 template <bool FROM_TABLE, class T, bool GROUPED>
-__global__ void __launch_bounds__(THREADS, 5)
-rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
+__global__ void __launch_bounds__(THREADS, RS_CTAS_PER_SM)
+rs_kernel(const ZsTile *__restrict__ tiles, const int32_t *__restrict__ order, int64_t tile0,
+          RankPtrs ptrs, int prefetch,
           const uint16_t *const *__restrict__ table, int32_t bucket0, int N, int G, float fN,
           uint16_t *__restrict__ gs, uint16_t *__restrict__ gP, double *__restrict__ partials) {
     __shared__ const uint16_t *sp[ZS_MAX_RANKS];
@@ -32,11 +43,11 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
     __shared__ int badw[WARPS];
     // the tile's results in destination order (the window of the tile norm)
     __shared__ __align__(16) uint16_t win[NORM_WIN_ELEMS];
-    const int64_t t = tile0 + blockIdx.x;
-    // the plan's tile table: written by copies only, never by a kernel, so
-    // it may be read before the wait below
+    // the plan's tables (written by copies only, never by a kernel, so they
+    // may be read before the wait below): this launch position's tile
+    const int64_t t = FROM_TABLE ? tile0 + blockIdx.x : (int64_t)order[tile0 + blockIdx.x];
     const ZsTile tile = tiles[t];
-    if (!FROM_TABLE && tile.valid > 0 && threadIdx.x < N) {
+    if (!FROM_TABLE && prefetch && tile.valid > 0 && threadIdx.x < N) {
         // A per-bucket launch is a programmatic dependent whose CTAs can be
         // placed while the previous kernel drains.  Meanwhile each of them
         // has the chunks that its first pass of the loop below reads (the
@@ -46,6 +57,9 @@ rs_kernel(const ZsTile *__restrict__ tiles, int64_t tile0, RankPtrs ptrs,
         // coherence, and the loads still come after the wait.  Fetching
         // the whole tile instead measured slower: the extra requests
         // compete with the loads of the CTAs that start after the wait.
+        // The host asks for it only when the bucket's CTAs fit in one wave
+        // (with more waves, most CTAs start after the wait, and it measured
+        // slower there too).
         const uint16_t *q = ptrs.p[threadIdx.x];
         if (q != nullptr && !(reinterpret_cast<uintptr_t>(q) & 15u)) {
             const int64_t lo = tile.src & ~int64_t(7);
@@ -406,12 +420,32 @@ norm_finish_kernel(const double *__restrict__ level1, int64_t n1, float max_norm
 
 using namespace zsk;
 
+// SM count of the current device, read once per device (atomic: host
+// threads may launch at once).
+static cudaError_t sm_count(int *out) {
+    static std::atomic<int> sms_of[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int sms = sms_of[dev].load(std::memory_order_relaxed);
+    if (sms <= 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (sms <= 0) sms = 1;
+        sms_of[dev].store(sms, std::memory_order_relaxed);
+    }
+    *out = sms;
+    return cudaSuccess;
+}
+
 // Per-bucket launches go out as programmatic dependents of the previous
 // kernel in the stream: back-to-back buckets then lose the launch gap
 // between them.  Stream order is kept: each CTA first waits for the
 // previous kernel (griddepcontrol.wait in rs_kernel).
 template <bool FROM_TABLE, class T, bool GROUPED>
-static cudaError_t launch_rs_pdl(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+static cudaError_t launch_rs_pdl(const ZsTile *d_tiles, const int32_t *d_order, int64_t tile0,
+                                 int64_t ntiles,
                                  const RankPtrs &p, const uint16_t *const *tbl, int N, int G,
                                  uint16_t *gs, uint16_t *gP, double *partials, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -424,37 +458,43 @@ static cudaError_t launch_rs_pdl(const ZsTile *d_tiles, int64_t tile0, int64_t n
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rs_kernel<FROM_TABLE, T, GROUPED>, d_tiles, tile0, p, tbl, 0, N, G,
+    int sms = 0;
+    const cudaError_t e = sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const int prefetch = ntiles <= (int64_t)sms * RS_CTAS_PER_SM ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, rs_kernel<FROM_TABLE, T, GROUPED>, d_tiles, d_order, tile0, p,
+                              prefetch, tbl, 0, N, G,
                               (float)N, gs, gP, partials);
 }
 
 template <class T>
-static cudaError_t launch_rs(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
+static cudaError_t launch_rs(const ZsTile *d_tiles, const int32_t *d_order, int64_t tile0,
+                             int64_t ntiles,
                              const RankPtrs &p, const void *const *d_table, int32_t bucket0, int N,
                              int G, uint16_t *gs,
                              uint16_t *gP, double *partials, cudaStream_t s) {
     const auto *tbl = reinterpret_cast<const uint16_t *const *>(d_table);
     const dim3 g((unsigned)ntiles), b(THREADS);
     if (d_table) {
-        if (G == N) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, bucket0, N, G, (float)N, gs, gP, partials);
-        else rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, tile0, p, tbl, bucket0, N, G, (float)N, gs, gP, partials);
+        if (G == N) rs_kernel<true, T, false><<<g, b, 0, s>>>(d_tiles, nullptr, tile0, p, 0, tbl, bucket0, N, G, (float)N, gs, gP, partials);
+        else rs_kernel<true, T, true><<<g, b, 0, s>>>(d_tiles, nullptr, tile0, p, 0, tbl, bucket0, N, G, (float)N, gs, gP, partials);
         return cudaGetLastError();
     }
     const cudaError_t e =
-        G == N ? launch_rs_pdl<false, T, false>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s)
-               : launch_rs_pdl<false, T, true>(d_tiles, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s);
+        G == N ? launch_rs_pdl<false, T, false>(d_tiles, d_order, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s)
+               : launch_rs_pdl<false, T, true>(d_tiles, d_order, tile0, ntiles, p, nullptr, N, G, gs, gP, partials, s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
-                               const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
+cudaError_t zsl_reduce_scatter(const ZsTile *d_tiles, const int32_t *d_order, int64_t tile0,
+                               int64_t ntiles, const void *const *rank_ptrs, int N, int G, int dtype, uint16_t *gs,
                                uint16_t *gP, double *partials, cudaStream_t s) {
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p;
     for (int k = 0; k < N; ++k) p.p[k] = static_cast<const uint16_t *>(rank_ptrs[k]);
     return dtype == ZS_DTYPE_FP16
-               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, nullptr, 0, N, G, gs, gP, partials, s)
-               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, nullptr, 0, N, G, gs, gP, partials, s);
+               ? launch_rs<FP16T>(d_tiles, d_order, tile0, ntiles, p, nullptr, 0, N, G, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, d_order, tile0, ntiles, p, nullptr, 0, N, G, gs, gP, partials, s);
 }
 
 cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t tile0, int64_t ntiles,
@@ -464,8 +504,8 @@ cudaError_t zsl_reduce_scatter_all(const ZsTile *d_tiles, int64_t tile0, int64_t
     if (ntiles <= 0) return cudaSuccess;
     RankPtrs p = {};
     return dtype == ZS_DTYPE_FP16
-               ? launch_rs<FP16T>(d_tiles, tile0, ntiles, p, d_table, bucket0, N, G, gs, gP, partials, s)
-               : launch_rs<BF16T>(d_tiles, tile0, ntiles, p, d_table, bucket0, N, G, gs, gP, partials, s);
+               ? launch_rs<FP16T>(d_tiles, nullptr, tile0, ntiles, p, d_table, bucket0, N, G, gs, gP, partials, s)
+               : launch_rs<BF16T>(d_tiles, nullptr, tile0, ntiles, p, d_table, bucket0, N, G, gs, gP, partials, s);
 }
 
 cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, int dtype,
@@ -473,20 +513,10 @@ cudaError_t zsl_norm(const ZsTile *d_tiles, int64_t ntiles, int64_t n_level1, in
                      float max_norm, float *d_norm, float *d_coef, int32_t *d_flags,
                      const ZsScaleArgs *scale, cudaStream_t s) {
     if (recompute && ntiles > 0) {
-        // persistent grid: NORM_CTAS_PER_SM CTAs on every SM (SM count per
-        // device, read once; atomic: host threads may launch at once)
-        static std::atomic<int> sms_of[64];
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+        // persistent grid: NORM_CTAS_PER_SM CTAs on every SM
+        int sms = 0;
+        const cudaError_t e = sm_count(&sms);
         if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        int sms = sms_of[dev].load(std::memory_order_relaxed);
-        if (sms <= 0) {
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess) return e;
-            if (sms <= 0) sms = 1;
-            sms_of[dev].store(sms, std::memory_order_relaxed);
-        }
         const int64_t warps = (ntiles + WARPS - 1) / WARPS;
         const int64_t grid = std::min<int64_t>(warps, (int64_t)sms * NORM_CTAS_PER_SM);
         if (dtype == ZS_DTYPE_FP16)
