@@ -261,8 +261,10 @@ zs_status zs_plan_table(const zs_plan *plan, void *host_out, int64_t bytes);
 /* Copy the plan's work tables to device memory owned by the caller
  * (d_table: 16-byte aligned, >= device_table_bytes).  Enqueued on stream;
  * the plan keeps d_table and uses it in every later device call, so it must
- * stay allocated while the plan is used.  Calling it again moves the plan
- * to the new buffer.  Errors: ZS_EINVAL, ZS_ECUDA. */
+ * stay allocated while the plan is used, and only this call may write it
+ * (zs_reduce_scatter reads it before waiting for the previous kernel of
+ * the stream).  Calling it again moves the plan to the new buffer.
+ * Errors: ZS_EINVAL, ZS_ECUDA. */
 zs_status zs_plan_upload(zs_plan *plan, void *d_table, int64_t bytes, void *stream);
 
 /* A1 data movement — partition full fp32 parameters (input space,
@@ -288,9 +290,11 @@ zs_status zs_partition(const zs_plan *plan, const float *full_params, const zs_s
  * not NULL (>= norm_scratch_elems doubles), the bucket's tiles also write
  * their sums of squared results there for zs_grad_norm.  The launch keeps
  * stream order: it waits for the previous kernel of the stream before
- * reading, so back-to-back calls each leave the GPU partly idle while the
- * previous bucket drains; zs_reduce_scatter_range takes several ready
- * buckets in one launch.  Errors: ZS_EINVAL (bucket out of range,
+ * reading rank_grads or writing anything, so back-to-back calls each leave
+ * the GPU partly idle while the previous bucket drains;
+ * zs_reduce_scatter_range takes several ready buckets in one launch.
+ * While it waits it may already have the start of its slice of every rank
+ * buffer fetched into L2, which changes no value it reads.  Errors: ZS_EINVAL (bucket out of range,
  * N > ZS_MAX_RANKS, NULL or misaligned pointer), ZS_ESTATE, ZS_ECUDA. */
 zs_status zs_reduce_scatter(const zs_plan *plan, int32_t bucket, const void *const *rank_grads,
                             void *grad_shards, void *persist_grads, double *norm_scratch,
