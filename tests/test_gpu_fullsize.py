@@ -306,3 +306,36 @@ def test_fullsize_whole_buckets(name):
         del dw
         gc.collect()
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["many_small", "llama3_8b", "llama3_8b_hsdp"])
+def test_fullsize_per_bucket_calls_equal_fused(name):
+    """zs_reduce_scatter bucket by bucket, at full size, gives the fused
+    launch's results bit for bit: every reduced gradient and every tile's
+    norm partial.  The per-bucket launches take each bucket's tiles largest
+    first; where a bucket's CTAs fit in one wave (the 8B lists) they also
+    prefetch their first pass into L2 while they wait on the previous
+    launch; many_small's buckets take several waves.  The fused launch is
+    the one test_fullsize_whole_buckets checks against the oracle."""
+    w = workloads.WORKLOADS[name]()
+    dw = bench.DeviceWorkload(w, "cuda:0", max_norm=w.max_norm)
+    try:
+        nt = dw.info["n_tiles"]
+        zs.zs_reduce_scatter_all(dw.plan, dw.ptr_table, dw.gs, dw.gP, dw.scratch)
+        torch.cuda.synchronize()
+        gs, gP = dw.gs.clone(), dw.gP.clone()
+        part = dw.scratch[:nt].clone()
+        # every element must be written again
+        dw.gs.fill_(-1)
+        dw.gP.fill_(-1)
+        dw.scratch.fill_(float("nan"))
+        for b in range(len(dw.buf_elems)):
+            zs.zs_reduce_scatter(dw.plan, b, dw.bucket_ptrs(b), dw.gs, dw.gP, dw.scratch)
+        torch.cuda.synchronize()
+        assert torch.equal(dw.gs, gs)
+        assert torch.equal(dw.gP, gP)
+        assert torch.equal(dw.scratch[:nt].view(torch.int64), part.view(torch.int64))
+    finally:
+        del dw
+        gc.collect()
+        torch.cuda.empty_cache()
