@@ -153,6 +153,27 @@ rs_kernel(const ZsTile *__restrict__ tiles, const int32_t *__restrict__ order, i
                         for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], T::to_f32(lane16(v, i)));
                     }
                 }
+            } else if (lo <= 0 && hi >= 8 && (G & 3) == 0) {
+                // HSDP, a full chunk and G a multiple of 4: each replica
+                // group's G ranks in rank order (loads in batches of 4),
+                // then the group sums in group order
+                for (int q0 = 0; q0 < N; q0 += G) {
+                    float in[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) in[i] = 0.0f;
+                    for (int k0 = q0; k0 < q0 + G; k0 += 4) {
+                        uint4 v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) v[u] = ldg16(p[k0 + u] + 8 * c);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                in[i] = __fadd_rn(in[i], T::to_f32(lane16(v[u], i)));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], in[i]);
+                }
             } else {
                 // HSDP: each replica group's G ranks in rank order, then the
                 // group sums in group order.  Loads go in batches of 4 ranks
