@@ -174,6 +174,33 @@ rs_kernel(const ZsTile *__restrict__ tiles, const int32_t *__restrict__ order, i
 #pragma unroll
                     for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], in[i]);
                 }
+            } else if (lo <= 0 && hi >= 8 && (N & 3) == 0) {
+                // HSDP, a full chunk, other G with N a multiple of 4: loads
+                // in batches of 4 ranks across group boundaries, no per-load
+                // conditions; the group boundary is a warp-uniform counter
+                float in[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) in[i] = 0.0f;
+                int cnt = 0;
+                for (int k0 = 0; k0 < N; k0 += 4) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[u] = ldg16(p[k0 + u] + 8 * c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            in[i] = __fadd_rn(in[i], T::to_f32(lane16(v[u], i)));
+                        if (++cnt == G) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                acc[i] = __fadd_rn(acc[i], in[i]);
+                                in[i] = 0.0f;
+                            }
+                            cnt = 0;
+                        }
+                    }
+                }
             } else {
                 // HSDP: each replica group's G ranks in rank order, then the
                 // group sums in group order.  Loads go in batches of 4 ranks
